@@ -1,0 +1,456 @@
+// api.cu -- the C ABI of libmoe.so (include/moe.h): configuration checks, workspace
+// layout, TMA tensor maps, and the stream-ordered launch sequence of moe_forward:
+//   route -> dispatch quantisation -> L1 GEMM (SwiGLU + requant) -> L2 GEMM
+//   [-> shared L1 -> shared L2] -> combine (+ shared) (+ RMSNorm).
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <new>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr int MAX_EXPERTS = 512;
+constexpr int MAX_TOP_K = 32;
+constexpr int MAX_HIDDEN = 16384;
+constexpr int64_t REGION_ALIGN = 1024;
+constexpr unsigned long long DEFAULT_TIMEOUT_NS = 2000000000ull;  // 2 s per bounded wait
+
+struct Dims {
+    int E, H, I, k, fmt, Is, sfmt;
+};
+
+Dims dims_of(const moe_config_t& c) {
+    return Dims{c.num_experts, c.hidden, c.inter, c.top_k, c.format, c.shared_inter, c.shared_format};
+}
+
+int validate(const moe_config_t* c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->format != MOE_FMT_BF16 && c->format != MOE_FMT_MXFP8 && c->format != MOE_FMT_NVFP4)
+        return MOE_ERR_UNSUPPORTED;
+    if (c->activation != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
+    if (c->num_experts < 1 || c->num_experts > MAX_EXPERTS) return MOE_ERR_INVALID_ARG;
+    if (c->top_k < 1 || c->top_k > c->num_experts || c->top_k > MAX_TOP_K) return MOE_ERR_INVALID_ARG;
+    if (c->max_tokens < 1) return MOE_ERR_INVALID_ARG;
+    if (c->hidden < 128 || c->inter < 128 || c->hidden % 128 || c->inter % 128) return MOE_ERR_INVALID_ARG;
+    if (c->hidden > MAX_HIDDEN) return MOE_ERR_INVALID_ARG;
+    if (c->format == MOE_FMT_NVFP4 && (c->hidden % 256 || c->inter % 256)) return MOE_ERR_INVALID_ARG;
+    if (!isfinite(c->act_alpha) || !isfinite(c->act_beta)) return MOE_ERR_INVALID_ARG;
+    if (c->act_has_clamp && !(c->act_clamp >= 0.0f)) return MOE_ERR_INVALID_ARG;
+    if (c->shared_inter < 0 || c->shared_inter % 128) return MOE_ERR_INVALID_ARG;
+    if (c->shared_inter > 0) {
+        if (c->shared_format != MOE_FMT_BF16 && c->shared_format != MOE_FMT_MXFP8) return MOE_ERR_UNSUPPORTED;
+        if (c->shared_format == MOE_FMT_BF16 && (c->hidden % 256 || c->shared_inter % 256))
+            return MOE_ERR_INVALID_ARG;
+    }
+    if (c->post_norm != 0 && c->post_norm != 1) return MOE_ERR_INVALID_ARG;
+    if (!isfinite(c->norm_eps) || c->norm_eps < 0.0f) return MOE_ERR_INVALID_ARG;
+    const int64_t R = (int64_t)c->max_tokens * c->top_k;
+    if (R + (int64_t)c->num_experts * BM >= (int64_t)1 << 30) return MOE_ERR_INVALID_ARG;  // int32 row indices
+    return MOE_OK;
+}
+
+// ------------------------------------------------------------------ workspace layout
+enum Region {
+    R_ERR, R_META, R_CNT, R_OFF, R_TILE_EXPERT, R_SRC, R_INV, R_XSCALE, R_XQ, R_XSF, R_HQ, R_HSF, R_Y, R_HDBG,
+    R_SXQ, R_SXSF, R_SHQ, R_SHSF, R_SY, R_COUNT
+};
+
+struct Layout {
+    int64_t off[R_COUNT];
+    int64_t size[R_COUNT];
+    int64_t total;
+    int64_t m_pad_max, m_tiles_max, t_pad;
+};
+
+Layout layout_of(const moe_config_t& c, int T) {
+    Layout L{};
+    const Dims d = dims_of(c);
+    const int64_t R = (int64_t)T * d.k;
+    L.m_pad_max = align_up(R + (int64_t)d.E * (BM - 1), BM);
+    if (L.m_pad_max == 0) L.m_pad_max = BM;
+    L.m_tiles_max = L.m_pad_max / BM;
+    L.t_pad = align_up(T > 0 ? T : 1, BM);
+    const int S = fmt_sf_atoms(d.fmt);
+    const int64_t nks_h = fmt_k_stages(d.fmt, d.H), nks_i = fmt_k_stages(d.fmt, d.I);
+    int64_t sz[R_COUNT] = {};
+    sz[R_ERR] = 16;
+    sz[R_META] = 16;
+    sz[R_CNT] = 4 * d.E;
+    sz[R_OFF] = 4 * (d.E + 1);
+    sz[R_TILE_EXPERT] = 4 * L.m_tiles_max;
+    sz[R_SRC] = 4 * L.m_pad_max;
+    sz[R_INV] = 4 * R;
+    sz[R_XSCALE] = 4 * (int64_t)T;
+    sz[R_XQ] = L.m_pad_max * fmt_row_bytes(d.fmt, d.H);
+    sz[R_XSF] = L.m_tiles_max * nks_h * S * ATOM_BYTES;
+    sz[R_HQ] = L.m_pad_max * fmt_row_bytes(d.fmt, d.I);
+    sz[R_HSF] = L.m_tiles_max * nks_i * S * ATOM_BYTES;
+    sz[R_Y] = L.m_pad_max * d.H * 2;
+    sz[R_HDBG] = (c.flags & MOE_FLAG_DEBUG_H) ? L.m_pad_max * d.I * 4 : 0;
+    if (d.Is > 0) {
+        const int Ss = fmt_sf_atoms(d.sfmt);
+        sz[R_SXQ] = L.t_pad * fmt_row_bytes(d.sfmt, d.H);
+        sz[R_SXSF] = (L.t_pad / BM) * fmt_k_stages(d.sfmt, d.H) * Ss * ATOM_BYTES;
+        sz[R_SHQ] = L.t_pad * fmt_row_bytes(d.sfmt, d.Is);
+        sz[R_SHSF] = (L.t_pad / BM) * fmt_k_stages(d.sfmt, d.Is) * Ss * ATOM_BYTES;
+        sz[R_SY] = L.t_pad * d.H * 2;
+    }
+    int64_t o = 0;
+    for (int r = 0; r < R_COUNT; ++r) {
+        L.off[r] = o;
+        L.size[r] = sz[r];
+        o += align_up(sz[r], REGION_ALIGN);
+    }
+    L.total = o;
+    return L;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// rows of row_bytes bytes, loaded as 128-byte x box_rows tiles with 128-byte swizzle
+bool map_2d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)BK_BYTES, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [E][N][row_bytes] weights, loaded as 128-byte x BN-row tiles of one expert
+bool map_3d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t N, uint64_t E) {
+    cuuint64_t dims[3] = {row_bytes, N, E};
+    cuuint64_t strides[2] = {row_bytes, row_bytes * N};
+    cuuint32_t box[3] = {(cuuint32_t)BK_BYTES, (cuuint32_t)BN, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+}  // namespace
+
+struct moe_plan_s {
+    moe_config_t cfg;
+    int device;
+    int num_sms;
+    unsigned long long timeout_ns;
+};
+
+#define CUDA_TRY(x)                              \
+    do {                                         \
+        if ((x) != cudaSuccess) return MOE_ERR_CUDA; \
+    } while (0)
+
+extern "C" {
+
+int moe_config_validate(const moe_config_t* cfg) { return validate(cfg); }
+
+int moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
+    if (!out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    const int v = validate(cfg);
+    if (v != MOE_OK) return v;
+    int dev = 0, major = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_UNSUPPORTED;
+    CUDA_TRY(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    if (major != 10) return MOE_ERR_UNSUPPORTED;
+    CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    if (!get_encode()) return MOE_ERR_CUDA;
+    CUDA_TRY(route_prepare(MAX_EXPERTS));
+    for (int f = MOE_FMT_BF16; f <= MOE_FMT_NVFP4; ++f) {
+        CUDA_TRY(gemm_prepare(f, true));
+        CUDA_TRY(gemm_prepare(f, false));
+    }
+    moe_plan_s* p = new (std::nothrow) moe_plan_s;
+    if (!p) return MOE_ERR_INVALID_ARG;
+    p->cfg = *cfg;
+    p->device = dev;
+    p->num_sms = sms;
+    p->timeout_ns = DEFAULT_TIMEOUT_NS;
+    *out = p;
+    return MOE_OK;
+}
+
+int moe_plan_destroy(moe_plan_t plan) {
+    delete plan;
+    return MOE_OK;
+}
+
+int moe_plan_block_m(moe_plan_t plan, int32_t num_tokens, int32_t* block_m) {
+    if (!plan || !block_m || num_tokens < 0) return MOE_ERR_INVALID_ARG;
+    *block_m = BM;
+    return MOE_OK;
+}
+
+int moe_config_workspace_size(const moe_config_t* cfg, int32_t num_tokens, size_t* bytes) {
+    const int v = validate(cfg);
+    if (v != MOE_OK) return v;
+    if (!bytes || num_tokens < 0) return MOE_ERR_INVALID_ARG;
+    if (num_tokens > cfg->max_tokens) return MOE_ERR_CAPACITY;
+    *bytes = (size_t)layout_of(*cfg, num_tokens).total;
+    return MOE_OK;
+}
+
+int moe_workspace_size(moe_plan_t plan, int32_t num_tokens, size_t* bytes) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    return moe_config_workspace_size(&plan->cfg, num_tokens, bytes);
+}
+
+int moe_workspace_region(moe_plan_t plan, int32_t num_tokens, int32_t which, size_t* offset, size_t* bytes) {
+    if (!plan || !offset || !bytes || num_tokens < 0) return MOE_ERR_INVALID_ARG;
+    static const int map[] = {R_CNT, R_OFF, R_SRC, R_INV, R_XQ, R_XSF, R_XSCALE, R_HQ, R_HSF, R_HDBG, R_Y, R_META, R_SY};
+    if (which < 0 || which >= (int)(sizeof(map) / sizeof(map[0]))) return MOE_ERR_INVALID_ARG;
+    const Layout L = layout_of(plan->cfg, num_tokens);
+    *offset = (size_t)L.off[map[which]];
+    *bytes = (size_t)L.size[map[which]];
+    return MOE_OK;
+}
+
+static int64_t weight_bytes(const moe_config_t& c, int which) {
+    const Dims d = dims_of(c);
+    const bool shared = which >= MOE_SHARED_W13 && which <= MOE_SHARED_W2_SF;
+    const int fmt = shared ? d.sfmt : d.fmt;
+    const int64_t E = shared ? 1 : d.E, I = shared ? d.Is : d.I, H = d.H;
+    if (shared && d.Is == 0) return 0;
+    const int S = fmt_sf_atoms(fmt);
+    switch (which) {
+        case MOE_W13:
+        case MOE_SHARED_W13: return E * 2 * I * fmt_row_bytes(fmt, H);
+        case MOE_W2:
+        case MOE_SHARED_W2: return E * H * fmt_row_bytes(fmt, I);
+        case MOE_W13_SF:
+        case MOE_SHARED_W13_SF: return E * ceil_div(2 * I, BN) * fmt_k_stages(fmt, H) * S * 2 * ATOM_BYTES;
+        case MOE_W2_SF:
+        case MOE_SHARED_W2_SF: return E * ceil_div(H, BN) * fmt_k_stages(fmt, I) * S * 2 * ATOM_BYTES;
+        case MOE_W13_GS:
+        case MOE_W2_GS: return d.fmt == MOE_FMT_NVFP4 ? 4 * E : 0;
+        default: return -1;
+    }
+}
+
+int moe_weight_layout_size(moe_plan_t plan, int32_t which, size_t* bytes) {
+    if (!plan || !bytes) return MOE_ERR_INVALID_ARG;
+    const int64_t b = weight_bytes(plan->cfg, which);
+    if (b < 0) return MOE_ERR_INVALID_ARG;
+    *bytes = (size_t)b;
+    return MOE_OK;
+}
+
+static int transform(const moe_config_t& c, int fmt, int E, int I, const moe_weights_t* src, moe_weights_t* dst,
+                     bool gscales, cudaStream_t st) {
+    const int H = c.hidden;
+    if (!src || !dst || !src->w13 || !src->w2 || !dst->w13 || !dst->w2) return MOE_ERR_INVALID_ARG;
+    if (!aligned(src->w13) || !aligned(src->w2) || !aligned(dst->w13) || !aligned(dst->w2)) return MOE_ERR_INVALID_ARG;
+    if (src->w13 == dst->w13 || src->w2 == dst->w2) return MOE_ERR_INVALID_ARG;
+    const bool scaled = fmt != MOE_FMT_BF16;
+    if (scaled && (!src->w13_sf || !src->w2_sf || !dst->w13_sf || !dst->w2_sf)) return MOE_ERR_INVALID_ARG;
+    if (gscales && fmt == MOE_FMT_NVFP4 && (!src->w13_gs || !src->w2_gs || !dst->w13_gs || !dst->w2_gs))
+        return MOE_ERR_INVALID_ARG;
+    CUDA_TRY(launch_interleave_rows((const uint8_t*)src->w13, (uint8_t*)dst->w13, E, I, fmt_row_bytes(fmt, H), st));
+    CUDA_TRY(cudaMemcpyAsync(dst->w2, src->w2, (size_t)E * H * fmt_row_bytes(fmt, I), cudaMemcpyDeviceToDevice, st));
+    if (scaled) {
+        CUDA_TRY(launch_pack_weight_sf((const uint8_t*)src->w13_sf, (uint8_t*)dst->w13_sf, fmt, E, 2 * I, H, true, I,
+                                       st));
+        CUDA_TRY(launch_pack_weight_sf((const uint8_t*)src->w2_sf, (uint8_t*)dst->w2_sf, fmt, E, H, I, false, I, st));
+    }
+    if (gscales && fmt == MOE_FMT_NVFP4) {
+        CUDA_TRY(cudaMemcpyAsync(dst->w13_gs, src->w13_gs, 4 * (size_t)E, cudaMemcpyDeviceToDevice, st));
+        CUDA_TRY(cudaMemcpyAsync(dst->w2_gs, src->w2_gs, 4 * (size_t)E, cudaMemcpyDeviceToDevice, st));
+    }
+    return MOE_OK;
+}
+
+int moe_transform_weights(moe_plan_t plan, const moe_weights_t* src, moe_weights_t* dst, void* stream) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    const moe_config_t& c = plan->cfg;
+    return transform(c, c.format, c.num_experts, c.inter, src, dst, true, (cudaStream_t)stream);
+}
+
+int moe_transform_shared_weights(moe_plan_t plan, const moe_weights_t* src, moe_weights_t* dst, void* stream) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    const moe_config_t& c = plan->cfg;
+    if (c.shared_inter == 0) return MOE_ERR_INVALID_ARG;
+    return transform(c, c.shared_format, 1, c.shared_inter, src, dst, false, (cudaStream_t)stream);
+}
+
+// one expert MLP pass (L1 then L2) over row tiles of the given A buffers
+static int run_mlp(const moe_plan_s* p, int fmt, int E, int I, int H, const void* xq, const uint8_t* xsf, int64_t rows,
+                   const moe_weights_t* w, const int* m_tiles_dev, int m_tiles_host, int64_t m_tiles_max,
+                   const int* tile_expert, const int* src, int m_valid, const float* x_scale, const float* a2,
+                   uint8_t* hq, uint8_t* hsf, float* h_debug, __nv_bfloat16* y, int* err, bool activation,
+                   cudaStream_t st) {
+    const moe_config_t& c = p->cfg;
+    CUtensorMap ta, tb;
+    GemmArgs g{};
+    g.m_tiles_dev = m_tiles_dev;
+    g.m_tiles_host = m_tiles_host;
+    g.tile_expert = tile_expert;
+    g.src = src;
+    g.m_valid = m_valid;
+    g.top_k = c.top_k;
+    g.err = err;
+    g.timeout_ns = p->timeout_ns;
+    g.act_alpha = activation ? c.act_alpha : 1.0f;
+    g.act_beta = activation ? c.act_beta : 0.0f;
+    g.act_clamp = c.act_clamp;
+    g.act_has_clamp = activation ? c.act_has_clamp : 0;
+    // L1: [rows, H] x w13[e]^T -> h [rows, I]
+    if (!map_2d(&ta, xq, fmt_row_bytes(fmt, H), rows, BM)) return MOE_ERR_CUDA;
+    if (!map_3d(&tb, w->w13, fmt_row_bytes(fmt, H), 2 * (uint64_t)I, E)) return MOE_ERR_CUDA;
+    g.sfa = xsf;
+    g.sfb = (const uint8_t*)w->w13_sf;
+    g.nks = (int)fmt_k_stages(fmt, H);
+    g.n_tiles = (int)ceil_div(2 * I, BN);
+    g.N = 2 * I;
+    g.x_scale = x_scale;
+    g.gscale = w->w13_gs;
+    g.a2 = a2;
+    g.hq = hq;
+    g.hsf = hsf;
+    g.I = I;
+    g.h_nks = (int)fmt_k_stages(fmt, I);
+    g.h_debug = h_debug;
+    const int grid1 = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, m_tiles_max * g.n_tiles));
+    CUDA_TRY(launch_gemm(fmt, true, ta, tb, g, grid1, st));
+    // L2: h [rows, I] x w2[e]^T -> y [rows, H]
+    if (!map_2d(&ta, hq, fmt_row_bytes(fmt, I), rows, BM)) return MOE_ERR_CUDA;
+    if (!map_3d(&tb, w->w2, fmt_row_bytes(fmt, I), H, E)) return MOE_ERR_CUDA;
+    g.sfa = hsf;
+    g.sfb = (const uint8_t*)w->w2_sf;
+    g.nks = (int)fmt_k_stages(fmt, I);
+    g.n_tiles = (int)ceil_div(H, BN);
+    g.N = H;
+    g.gscale = w->w2_gs;
+    g.y = y;
+    g.ldy = H;
+    const int grid2 = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, m_tiles_max * g.n_tiles));
+    CUDA_TRY(launch_gemm(fmt, false, ta, tb, g, grid2, st));
+    return MOE_OK;
+}
+
+int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* topk_ids, const float* topk_weights,
+                const moe_weights_t* weights, const float* l2_act_scale, const moe_weights_t* shared,
+                const float* norm_gamma, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    const moe_config_t& c = plan->cfg;
+    const Dims d = dims_of(c);
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (T > c.max_tokens) return MOE_ERR_CAPACITY;
+    if (T == 0) return MOE_OK;
+    if (!hidden || !topk_ids || !topk_weights || !weights || !out || !workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned(hidden) || !aligned(topk_ids) || !aligned(topk_weights) || !aligned(out) || !aligned(workspace))
+        return MOE_ERR_INVALID_ARG;
+    if (out == hidden) return MOE_ERR_INVALID_ARG;
+    if (!weights->w13 || !weights->w2) return MOE_ERR_INVALID_ARG;
+    if (d.fmt != MOE_FMT_BF16 && (!weights->w13_sf || !weights->w2_sf)) return MOE_ERR_INVALID_ARG;
+    if (d.fmt == MOE_FMT_NVFP4 && (!weights->w13_gs || !weights->w2_gs || !l2_act_scale)) return MOE_ERR_INVALID_ARG;
+    if (d.Is > 0 && (!shared || !shared->w13 || !shared->w2)) return MOE_ERR_INVALID_ARG;
+    if (d.Is > 0 && d.sfmt != MOE_FMT_BF16 && (!shared->w13_sf || !shared->w2_sf)) return MOE_ERR_INVALID_ARG;
+    if (c.post_norm && !norm_gamma) return MOE_ERR_INVALID_ARG;
+    const Layout L = layout_of(c, T);
+    if (workspace_bytes < (size_t)L.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t* ws = (uint8_t*)workspace;
+    auto R = [&](int r) { return ws + L.off[r]; };
+    int* err = (int*)R(R_ERR);
+    int* meta = (int*)R(R_META);
+    CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int), st));  // the status reflects this call only
+
+    CUDA_TRY(launch_route(topk_ids, T, d.k, d.E, (int*)R(R_CNT), (int*)R(R_OFF), (int*)R(R_SRC), (int*)R(R_INV),
+                          (int*)R(R_TILE_EXPERT), meta, err, st));
+    DispatchArgs da{};
+    da.x = (const uint16_t*)hidden;
+    da.T = T;
+    da.H = d.H;
+    da.k = d.k;
+    da.inv = (const int*)R(R_INV);
+    da.fmt = d.fmt;
+    da.xq = R(R_XQ);
+    da.xsf = R(R_XSF);
+    da.x_scale = (float*)R(R_XSCALE);
+    da.shared_fmt = d.Is > 0 ? d.sfmt : -1;
+    da.sxq = R(R_SXQ);
+    da.sxsf = R(R_SXSF);
+    CUDA_TRY(launch_dispatch(da, st));
+
+    int rc = run_mlp(plan, d.fmt, d.E, d.I, d.H, R(R_XQ), R(R_XSF), L.m_pad_max, weights, meta + 1, 0, L.m_tiles_max,
+                     (const int*)R(R_TILE_EXPERT), (const int*)R(R_SRC), 0, (const float*)R(R_XSCALE), l2_act_scale,
+                     R(R_HQ), R(R_HSF), (c.flags & MOE_FLAG_DEBUG_H) ? (float*)R(R_HDBG) : nullptr,
+                     (__nv_bfloat16*)R(R_Y), err, true, st);
+    if (rc != MOE_OK) return rc;
+    if (d.Is > 0) {
+        const int tiles = (int)(L.t_pad / BM);
+        rc = run_mlp(plan, d.sfmt, 1, d.Is, d.H, R(R_SXQ), R(R_SXSF), L.t_pad, shared, nullptr, tiles, tiles, nullptr,
+                     nullptr, T, nullptr, nullptr, R(R_SHQ), R(R_SHSF), nullptr, (__nv_bfloat16*)R(R_SY), err, false,
+                     st);
+        if (rc != MOE_OK) return rc;
+    }
+    CombineArgs ca{};
+    ca.y = (const __nv_bfloat16*)R(R_Y);
+    ca.inv = (const int*)R(R_INV);
+    ca.w = topk_weights;
+    ca.T = T;
+    ca.k = d.k;
+    ca.H = d.H;
+    ca.ys = d.Is > 0 ? (const __nv_bfloat16*)R(R_SY) : nullptr;
+    ca.gamma = c.post_norm ? norm_gamma : nullptr;
+    ca.eps = c.norm_eps;
+    ca.out = (__nv_bfloat16*)out;
+    CUDA_TRY(launch_combine(ca, st));
+    return MOE_OK;
+}
+
+int moe_last_status(moe_plan_t plan, void* workspace, void* stream, int32_t* status) {
+    if (!plan || !workspace || !status) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    int v = 0;
+    CUDA_TRY(cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(cudaStreamSynchronize(st));
+    CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(int), st));
+    CUDA_TRY(cudaStreamSynchronize(st));
+    *status = v;
+    return MOE_OK;
+}
+
+const char* moe_error_string(int32_t status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, or unsupported shape)";
+        case MOE_ERR_UNSUPPORTED: return "unsupported device, format or activation";
+        case MOE_ERR_CAPACITY: return "num_tokens exceeds max_tokens";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_BAD_EXPERT_ID: return "expert id outside [-1, num_experts)";
+        case MOE_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

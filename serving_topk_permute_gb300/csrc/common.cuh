@@ -1,0 +1,288 @@
+// common.cuh -- shared device helpers for the sm_103a MoE kernels: inline PTX for
+// mbarriers (bounded waits), TMA / bulk copies, tcgen05 (tensor memory, MMA,
+// scale-factor copies, loads), FP8 / FP4 conversions, and the layout formulas
+// every kernel agrees on.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ tile geometry
+constexpr int BM = 128;            // rows per MMA tile (= BLOCK_M of the routing)
+constexpr int BN = 256;            // columns per MMA tile (weight rows)
+constexpr int BK_BYTES = 128;      // bytes of codes per K stage (one 128-byte swizzle row)
+constexpr int ATOM_BYTES = 512;    // one scale-factor atom: 128 rows x 4 scales
+constexpr int NUM_STAGES = 4;
+constexpr int GEMM_THREADS = 192;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 epilogue
+constexpr int TMEM_COLS = 512;
+constexpr int ACC_COLS = BN;       // fp32 accumulator columns
+
+// per-format constants
+__host__ __device__ constexpr int fmt_elem_bits(int fmt) { return fmt == MOE_FMT_BF16 ? 16 : (fmt == MOE_FMT_MXFP8 ? 8 : 4); }
+// scale-factor atoms per K stage (each atom covers 4 scale blocks along K)
+__host__ __device__ constexpr int fmt_sf_atoms(int fmt) { return fmt == MOE_FMT_BF16 ? 0 : (fmt == MOE_FMT_MXFP8 ? 1 : 4); }
+// elements per scale block
+__host__ __device__ constexpr int fmt_sf_block(int fmt) { return fmt == MOE_FMT_MXFP8 ? 32 : 16; }
+// bytes of one row of K elements
+__host__ __device__ inline int64_t fmt_row_bytes(int fmt, int64_t K) { return K * fmt_elem_bits(fmt) / 8; }
+// number of 128-byte K stages for K elements
+__host__ __device__ inline int64_t fmt_k_stages(int fmt, int64_t K) { return fmt_row_bytes(fmt, K) / BK_BYTES; }
+
+// Byte offset of scale block kb of row r in an activation scale-atom array laid
+// out [row tile][K stage][S atoms][512]: within an atom, row m = 32j + i and
+// scale b (of 4) sit at byte 16i + 4j + b.
+__host__ __device__ inline int64_t act_sf_offset(int64_t r, int64_t kb, int S, int64_t nks) {
+    const int64_t mt = r / BM, m = r % BM;
+    const int64_t ks = kb / (4 * S), s = (kb / 4) % S, b = kb % 4;
+    return ((mt * nks + ks) * S + s) * ATOM_BYTES + (m % 32) * 16 + (m / 32) * 4 + b;
+}
+
+// Byte offset of scale block kb of kernel-layout weight row n of expert e in a
+// weight scale-atom array laid out [E][N tiles][K stage][S atoms][2 halves][512].
+__host__ __device__ inline int64_t wt_sf_offset(int64_t e, int64_t n, int64_t kb, int S, int64_t nks,
+                                                int64_t n_tiles) {
+    const int64_t nt = n / BN, nb = (n % BN) / BM, m = n % BM;
+    const int64_t ks = kb / (4 * S), s = (kb / 4) % S, b = kb % 4;
+    return ((((e * n_tiles + nt) * nks + ks) * S + s) * 2 + nb) * ATOM_BYTES + (m % 32) * 16 + (m / 32) * 4 + b;
+}
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ inline int64_t align_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// ------------------------------------------------------------------ device error word
+__device__ inline void set_error(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ------------------------------------------------------------------ shared memory / mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with parity `parity` to complete, giving up after
+// timeout_ns (or as soon as *abort is set). Returns false on give-up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                          const volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+// ------------------------------------------------------------------ TMA / bulk copies (global -> shared)
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+// plain bulk copy: both addresses 16-byte aligned, bytes a multiple of 16
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// arrive on `bar` once every tcgen05 operation issued so far by this thread has completed
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start >> 4 in bits 0-13,
+// leading byte offset >> 4 in 16-29, stride byte offset >> 4 in 32-45, the
+// fixed 0b001 in 46-48, swizzle mode in 61-63 (2 = 128-byte swizzle, 0 = none).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)(swizzle & 7) << 61;
+    return d;
+}
+
+// K-major operand tile whose rows are 128 bytes, 128-byte swizzled (as TMA
+// writes it): 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) { return smem_desc(saddr, 16, 1024, 2); }
+
+// 32 rows x 16 bytes, no swizzle (the source of a 32x128b tensor-memory copy)
+__device__ __forceinline__ uint64_t sf_atom_desc(uint32_t saddr) { return smem_desc(saddr, 0, 128, 0); }
+
+// copy one scale-factor atom (32 lanes x 128 bits, replicated to the four lane quarters)
+__device__ __forceinline__ void tc_cp_sf_atom(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptors (M = 128, N = BN, both operands K-major).
+// kind::f16: D fp32 (bits 4-5 = 1), A/B bf16 (bits 7-9, 10-12 = 1), N>>3 at 17, M>>4 at 24.
+__host__ __device__ constexpr uint32_t idesc_bf16() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+// kind::mxf8f6f4: A/B E4M3 (0), scale type UE8M0 (bit 23), scale ids: B at 4-5, A at 29-30.
+__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t sf_id) {
+    return (sf_id << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
+}
+// kind::mxf4nvf4: A/B E2M1 (1), scale type UE4M3 (bit 23 = 0).
+__host__ __device__ constexpr uint32_t idesc_nvf4() {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+// load 32 consecutive fp32 columns of this warp's 32 lanes (one row per thread)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ conversions
+// two fp32 -> packed E4M3 pair, round to nearest even, saturate to +-448; `lo` goes to the low byte
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// two fp32 -> packed E2M1 pair, round to nearest even, saturate to +-6; `lo` goes to the low nibble
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+// one E4M3 byte -> fp32 (exact)
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+    uint32_t h2;
+    const uint16_t in = (uint16_t)((byte & 0xFF) | ((byte & 0xFF) << 8));  // same code in both halves
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
+}
+
+// UE8M0 exponent of a block: the smallest e with amax <= 448 * 2^e (0 for amax == 0),
+// decided exactly from frexp: amax = f * 2^p, f in [0.5, 1), 448 = 0.875 * 2^9.
+__device__ __forceinline__ int ue8m0_exponent(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    int p;
+    const float f = frexpf(amax, &p);
+    int e = (f <= 0.875f) ? p - 9 : p - 8;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+}  // namespace moe

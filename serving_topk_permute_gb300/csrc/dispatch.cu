@@ -1,0 +1,170 @@
+// dispatch.cu -- dispatch-side activation quantisation fused with the permute
+// (vllm.model_executor.layers.fused_moe.deep_gemm_mega_moe, module docstring and
+// DeepGemmMegaMoEExperts.forward: prepare_megamoe_inputs quantises hidden once
+// per token; vllm.model_executor.layers.fused_moe, DeepGemmExperts.apply:
+// deepgemm_moe_permute writes a1q_perm).
+//
+// One CTA of 128 threads per token. Each thread owns 8-element chunks
+// c = tid + 128 i of the row, loaded as one 128-bit bf16x8 vector each, kept in
+// registers. Per format:
+//   BF16   the 16-byte chunk is copied as is
+//   MXFP8  a 32-element block is 4 neighbouring threads: block amax by two xor
+//          shuffles, e = smallest integer with amax <= 448 * 2^e, codes
+//          E4M3(x * 2^-e) (RNE, saturating), scale byte e + 127
+//   NVFP4  token amax by a block reduction, token scale gs = amax / 2688 (fp32),
+//          a 16-element block is 2 neighbouring threads: block scale
+//          sb = E4M3(amax_b / (gs * 6)), eff = value(sb) * gs, codes E2M1(x / eff)
+//          packed two per byte (element 2i in the low nibble), all in fp32 RN
+// The codes are written to each of the token's k permuted rows (inv_perm), and
+// the scale bytes to the matching position of the 128-row scale atoms the MMA
+// reads. With a shared expert, the token is also quantised to the shared format
+// into row t of a separate (unpermuted) buffer.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int DISPATCH_THREADS = 128;
+constexpr int DISPATCH_MAX_CHUNKS = 16;  // H <= 16 * 128 * 8 = 16384
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// MXFP8 codes of one 8-element chunk (block exponent ex), as 8 bytes
+__device__ __forceinline__ uint2 mxfp8_chunk(const float (&f)[8], int ex) {
+    uint32_t w[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t lo = cvt_e4m3x2(ldexpf(f[4 * i], -ex), ldexpf(f[4 * i + 1], -ex));
+        const uint32_t hi = cvt_e4m3x2(ldexpf(f[4 * i + 2], -ex), ldexpf(f[4 * i + 3], -ex));
+        w[i] = lo | (hi << 16);
+    }
+    return make_uint2(w[0], w[1]);
+}
+
+// block exponent of the 32-element block held by 4 neighbouring lanes
+__device__ __forceinline__ int mxfp8_block_exponent(const float (&f)[8]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    return ue8m0_exponent(amax);
+}
+
+__global__ void __launch_bounds__(DISPATCH_THREADS)
+    dispatch_kernel(const DispatchArgs a) {
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+    const int nchunks = a.H / 8;
+    __shared__ int s_rows[32];
+    __shared__ float s_amax[DISPATCH_THREADS / 32];
+
+    if (tid < a.k) s_rows[tid] = a.inv[(int64_t)t * a.k + tid];
+
+    // load the token's row into registers
+    uint4 v[DISPATCH_MAX_CHUNKS];
+    const uint4* xrow = reinterpret_cast<const uint4*>(a.x + (int64_t)t * a.H);
+#pragma unroll
+    for (int i = 0; i < DISPATCH_MAX_CHUNKS; ++i) {
+        const int c = tid + i * DISPATCH_THREADS;
+        v[i] = c < nchunks ? xrow[c] : make_uint4(0, 0, 0, 0);
+    }
+
+    // NVFP4: the token's own scale
+    float gs = 1.0f;
+    if (a.fmt == MOE_FMT_NVFP4) {
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < DISPATCH_MAX_CHUNKS; ++i) {
+            float f[8];
+            bf16x8_to_f32(v[i], f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) s_amax[warp] = amax;
+        __syncthreads();
+        amax = s_amax[0];
+#pragma unroll
+        for (int w = 1; w < DISPATCH_THREADS / 32; ++w) amax = fmaxf(amax, s_amax[w]);
+        gs = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+        if (tid == 0) a.x_scale[t] = gs;
+    } else {
+        __syncthreads();
+    }
+    const int k = a.k;
+    const int64_t nks_x = fmt_k_stages(a.fmt, a.H);
+
+#pragma unroll
+    for (int i = 0; i < DISPATCH_MAX_CHUNKS; ++i) {
+        const int c = tid + i * DISPATCH_THREADS;
+        if (i * DISPATCH_THREADS >= nchunks) break;  // uniform across the CTA
+        const bool in = c < nchunks;
+        float f[8];
+        bf16x8_to_f32(v[i], f);
+        if (a.fmt == MOE_FMT_BF16) {
+            if (in)
+                for (int j = 0; j < k; ++j) {
+                    const int r = s_rows[j];
+                    if (r >= 0) reinterpret_cast<uint4*>(a.xq + (int64_t)r * a.H * 2)[c] = v[i];
+                }
+        } else if (a.fmt == MOE_FMT_MXFP8) {
+            const int ex = mxfp8_block_exponent(f);
+            const uint2 codes = mxfp8_chunk(f, ex);
+            if (in)
+                for (int j = 0; j < k; ++j) {
+                    const int r = s_rows[j];
+                    if (r < 0) continue;
+                    reinterpret_cast<uint2*>(a.xq + (int64_t)r * a.H)[c] = codes;
+                    if ((c & 3) == 0) a.xsf[act_sf_offset(r, c / 4, 1, nks_x)] = (uint8_t)(ex + 127);
+                }
+        } else {
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            const uint32_t sb = cvt_e4m3x2(__fdiv_rn(amax, __fmul_rn(gs, 6.0f)), 0.0f) & 0xFF;
+            const float eff = __fmul_rn(e4m3_to_f32(sb), gs);
+            uint32_t word = 0;
+            if (eff > 0.0f) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    word |= cvt_e2m1x2(__fdiv_rn(f[2 * j], eff), __fdiv_rn(f[2 * j + 1], eff)) << (8 * j);
+            }
+            if (in)
+                for (int j = 0; j < k; ++j) {
+                    const int r = s_rows[j];
+                    if (r < 0) continue;
+                    reinterpret_cast<uint32_t*>(a.xq + (int64_t)r * (a.H / 2))[c] = word;
+                    if ((c & 1) == 0) a.xsf[act_sf_offset(r, c / 2, 4, nks_x)] = (uint8_t)sb;
+                }
+        }
+        // unpermuted copy for the shared expert
+        if (a.shared_fmt == MOE_FMT_BF16) {
+            if (in) reinterpret_cast<uint4*>(a.sxq + (int64_t)t * a.H * 2)[c] = v[i];
+        } else if (a.shared_fmt == MOE_FMT_MXFP8) {
+            const int ex = mxfp8_block_exponent(f);
+            const uint2 codes = mxfp8_chunk(f, ex);
+            if (in) {
+                reinterpret_cast<uint2*>(a.sxq + (int64_t)t * a.H)[c] = codes;
+                if ((c & 3) == 0)
+                    a.sxsf[act_sf_offset(t, c / 4, 1, fmt_k_stages(MOE_FMT_MXFP8, a.H))] = (uint8_t)(ex + 127);
+            }
+        }
+    }
+}
+
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st) {
+    dispatch_kernel<<<a.T, DISPATCH_THREADS, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

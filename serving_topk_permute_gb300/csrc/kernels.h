@@ -1,0 +1,90 @@
+// kernels.h -- internal host-side launchers of the MoE kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ------------------------------------------------------------------ routing
+// Histogram, BLOCK_M-padded offsets, stable scatter (one CTA). Writes cnt[E],
+// off[E+1], src[M_pad] (-1 padding), inv[T*k] (-1 masked), tile_expert[M_pad/BM],
+// meta[0] = M_pad, meta[1] = M_pad / BM.
+size_t route_smem_bytes(int E);
+cudaError_t route_prepare(int E);   // sets the dynamic shared memory attribute (E <= 512)
+cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int* cnt, int* off, int* src, int* inv,
+                         int* tile_expert, int* meta, int* err, cudaStream_t st);
+
+// ------------------------------------------------------------------ dispatch quantisation
+struct DispatchArgs {
+    const uint16_t* x;   // bf16 bits [T, H]
+    int T, H, k;
+    const int* inv;      // [T*k] permuted row of each slot (-1 = masked)
+    int fmt;             // routed format
+    uint8_t* xq;         // [M_pad_max, H/vpe] permuted rows
+    uint8_t* xsf;        // scale atoms
+    float* x_scale;      // [T] NVFP4 per-token scale
+    int shared_fmt;      // -1: no shared copy
+    uint8_t* sxq;        // [T_pad, H/vpe] identity rows
+    uint8_t* sxsf;
+};
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st);
+
+// ------------------------------------------------------------------ grouped GEMM
+struct GemmArgs {
+    const uint8_t* sfa;        // activation scale atoms [row tiles][nks][S][512]
+    const uint8_t* sfb;        // weight scale atoms [E][n_tiles][nks][S][2][512]
+    int nks;                   // 128-byte K stages
+    int n_tiles;               // 256-column tiles
+    int N;                     // output columns (kernel-layout weight rows)
+    const int* m_tiles_dev;    // number of 128-row tiles on the device (or null)
+    int m_tiles_host;          // used when m_tiles_dev is null
+    const int* tile_expert;    // expert of each row tile (null: expert 0)
+    const int* src;            // flat slot of each row, -1 = padding (null: rows < m_valid are valid)
+    int m_valid;
+    int top_k;
+    const float* x_scale;      // NVFP4 L1: per-token dispatch scale [T]
+    const float* gscale;       // NVFP4: per-expert global weight scale [E]
+    const float* a2;           // NVFP4: device scalar, the L2 input scale
+    // L1 epilogue output (the L2 input)
+    uint8_t* hq;
+    uint8_t* hsf;
+    int I;
+    int h_nks;
+    float* h_debug;
+    float act_alpha, act_beta, act_clamp;
+    int act_has_clamp;
+    // L2 epilogue output
+    __nv_bfloat16* y;
+    int ldy;
+    int* err;
+    unsigned long long timeout_ns;
+};
+size_t gemm_smem_bytes(int fmt);
+cudaError_t gemm_prepare(int fmt, bool l1);   // sets the dynamic shared memory attribute
+cudaError_t launch_gemm(int fmt, bool l1, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                        int grid, cudaStream_t st);
+
+// ------------------------------------------------------------------ combine
+struct CombineArgs {
+    const __nv_bfloat16* y;    // [M_pad_max, H] per-row L2 output
+    const int* inv;            // [T*k]
+    const float* w;            // [T*k]
+    int T, k, H;
+    const __nv_bfloat16* ys;   // [T, H] shared expert output or null
+    const float* gamma;        // [H] or null
+    float eps;
+    __nv_bfloat16* out;        // [T, H]
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+
+// ------------------------------------------------------------------ weight transform
+cudaError_t launch_interleave_rows(const uint8_t* src, uint8_t* dst, int E, int I, int64_t row_bytes,
+                                   cudaStream_t st);
+// scale atoms from row-major [E, N, K/g] u8 scales; interleave: apply the w13 row interleave
+cudaError_t launch_pack_weight_sf(const uint8_t* src, uint8_t* dst, int fmt, int E, int N, int K, bool interleave,
+                                  int I, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,138 @@
+// routing.cu -- per-expert histogram, BLOCK_M-padded segment offsets and the stable
+// scatter of routed slots into them (vllm.model_executor.layers.fused_moe,
+// DeepGemmExperts.workspace_shapes: compute_aligned_M, M_sum % block_m == 0;
+// DeepGemmExperts.apply: deepgemm_moe_permute -> expert ids and inv_perm).
+//
+// One CTA of 1024 threads (32 warps). Warp w owns a contiguous chunk of the
+// flat slots s = t*k + j.
+//   pass 1  each warp counts its chunk per expert into its own shared row
+//   scan    per expert: exclusive prefix over warps (a warp's base inside the
+//           expert) and the total; padded sizes; a block-wide scan gives the
+//           segment offsets
+//   pass 2  each warp walks its chunk in ascending order, 32 slots at a time;
+//           __match_any_sync groups lanes with the same expert, the rank inside
+//           the group plus the warp's running count gives the row. Rows inside
+//           a segment are therefore ordered by ascending slot: a stable scatter.
+// Integer-only and deterministic. Ids outside [-1, E) set MOE_ERR_BAD_EXPERT_ID
+// and are treated as masked.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int ROUTE_THREADS = 1024;
+constexpr int ROUTE_WARPS = ROUTE_THREADS / 32;
+
+__global__ void __launch_bounds__(ROUTE_THREADS, 1)
+    route_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int* __restrict__ cnt, int* __restrict__ off,
+                 int* __restrict__ src, int* __restrict__ inv, int* __restrict__ tile_expert, int* __restrict__ meta,
+                 int* err) {
+    extern __shared__ int sm[];
+    int* wcnt = sm;                          // [32][E]: per-warp counts, then per-warp running bases
+    int* s_off = sm + ROUTE_WARPS * E;       // [E+1]
+    int* s_cnt = s_off + (E + 1);            // [E]
+    int* s_wsum = s_cnt + E;                 // [32] scan scratch
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int R = T * k;
+    const int chunk = (int)align_up(ceil_div(R, ROUTE_WARPS), 32);
+    const int beg = min(warp * chunk, R), end = min(beg + chunk, R);
+
+    for (int i = tid; i < ROUTE_WARPS * E; i += ROUTE_THREADS) wcnt[i] = 0;
+    __syncthreads();
+
+    // pass 1: per-warp histograms
+    for (int s = beg + lane; s < end; s += 32) {
+        const int e = ids[s];
+        if (e >= 0 && e < E)
+            atomicAdd(&wcnt[warp * E + e], 1);
+        else if (e != -1)
+            set_error(err, MOE_ERR_BAD_EXPERT_ID);
+    }
+    __syncthreads();
+
+    // per expert: exclusive prefix over warps, total, padded size
+    for (int e = tid; e < E; e += ROUTE_THREADS) {
+        int run = 0;
+        for (int w = 0; w < ROUTE_WARPS; ++w) {
+            const int c = wcnt[w * E + e];
+            wcnt[w * E + e] = run;
+            run += c;
+        }
+        s_cnt[e] = run;
+        cnt[e] = run;
+    }
+    __syncthreads();
+
+    // block-wide exclusive scan of the padded sizes (E <= 1024: one value per thread)
+    {
+        const int v = tid < E ? (int)align_up(s_cnt[tid], BM) : 0;
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = s_wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            s_wsum[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        const int incl = x + (warp > 0 ? s_wsum[warp - 1] : 0);
+        if (tid < E) s_off[tid] = incl - v;
+        if (tid == E - 1) s_off[E] = incl;
+    }
+    __syncthreads();
+    for (int e = tid; e <= E; e += ROUTE_THREADS) off[e] = s_off[e];
+
+    // pass 2: stable scatter
+    const unsigned lt = (1u << lane) - 1u;
+    for (int s0 = beg; s0 < end; s0 += 32) {
+        const int s = s0 + lane;
+        const int e = s < end ? ids[s] : -1;
+        const bool routed = s < end && e >= 0 && e < E;
+        const int key = routed ? e : E + lane;  // unrouted lanes never group
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (routed) {
+            const int row = s_off[e] + wcnt[warp * E + e] + __popc(peers & lt);
+            src[row] = s;
+            inv[s] = row;
+        } else if (s < end) {
+            inv[s] = -1;
+        }
+        __syncwarp();
+        if (routed && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+        __syncwarp();
+    }
+
+    // padding rows and the row-tile -> expert map
+    for (int e = tid; e < E; e += ROUTE_THREADS) {
+        for (int r = s_off[e] + s_cnt[e]; r < s_off[e + 1]; ++r) src[r] = -1;
+        for (int mt = s_off[e] / BM; mt < s_off[e + 1] / BM; ++mt) tile_expert[mt] = e;
+    }
+    if (tid == 0) {
+        meta[0] = s_off[E];
+        meta[1] = s_off[E] / BM;
+    }
+}
+
+size_t route_smem_bytes(int E) { return sizeof(int) * ((size_t)ROUTE_WARPS * E + (E + 1) + E + 32); }
+
+cudaError_t route_prepare(int E) {
+    return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)route_smem_bytes(E));
+}
+
+cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int* cnt, int* off, int* src, int* inv,
+                         int* tile_expert, int* meta, int* err, cudaStream_t st) {
+    const size_t smem = route_smem_bytes(E);
+    route_kernel<<<1, ROUTE_THREADS, smem, st>>>(ids, T, k, E, cnt, off, src, inv, tile_expert, meta, err);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,241 @@
+"""Thin Python binding of libmoe.so (include/moe.h): argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; PyTorch only
+provides device memory (tensors) and the current stream. If the library is
+missing this module raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libmoe.so")
+_lib = None
+
+MOE_OK = 0
+FORMATS = {"bf16": 0, "mxfp8": 1, "nvfp4": 2}
+
+# weight tensor ids (moe_weight_layout_size)
+W13, W13_SF, W2, W2_SF, SHARED_W13, SHARED_W13_SF, SHARED_W2, SHARED_W2_SF, W13_GS, W2_GS = range(10)
+# workspace regions (moe_workspace_region)
+REGIONS = {"counts": 0, "offsets": 1, "src": 2, "inv_perm": 3, "xq": 4, "xsf": 5, "x_scale": 6, "hq": 7,
+           "hsf": 8, "h_debug": 9, "y": 10, "meta": 11, "shared_y": 12}
+FLAG_DEBUG_H = 1
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status} ({error_string(status)})")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("num_experts", ctypes.c_int32), ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("format", ctypes.c_int32),
+                ("activation", ctypes.c_int32), ("act_alpha", ctypes.c_float), ("act_beta", ctypes.c_float),
+                ("act_clamp", ctypes.c_float), ("act_has_clamp", ctypes.c_int32),
+                ("shared_inter", ctypes.c_int32), ("shared_format", ctypes.c_int32),
+                ("post_norm", ctypes.c_int32), ("norm_eps", ctypes.c_float), ("flags", ctypes.c_uint32)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("w13", ctypes.c_void_p), ("w13_sf", ctypes.c_void_p), ("w13_gs", ctypes.c_void_p),
+                ("w2", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p), ("w2_gs", ctypes.c_void_p)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libmoe.so is not built ({_LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        sigs = {
+            "moe_config_validate": [P],
+            "moe_plan": [P, P],
+            "moe_plan_destroy": [P],
+            "moe_plan_block_m": [P, I32, P],
+            "moe_workspace_size": [P, I32, P],
+            "moe_config_workspace_size": [P, I32, P],
+            "moe_weight_layout_size": [P, I32, P],
+            "moe_transform_weights": [P, P, P, P],
+            "moe_transform_shared_weights": [P, P, P, P],
+            "moe_forward": [P, I32, P, P, P, P, P, P, P, P, P, SZ, P],
+            "moe_last_status": [P, P, P, P],
+            "moe_workspace_region": [P, I32, I32, P, P],
+        }
+        for name, args in sigs.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.moe_error_string.argtypes = [I32]
+        L.moe_error_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def error_string(status: int) -> str:
+    return lib().moe_error_string(status).decode()
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+@dataclass
+class LayerConfig:
+    num_experts: int
+    hidden: int
+    inter: int
+    top_k: int
+    max_tokens: int
+    fmt: str = "bf16"
+    act_alpha: float = 1.0
+    act_beta: float = 0.0
+    act_clamp: float | None = None
+    shared_inter: int = 0
+    shared_fmt: str = "mxfp8"
+    post_norm: bool = False
+    norm_eps: float = 1e-6
+    debug_h: bool = False
+
+    def to_c(self) -> Config:
+        return Config(self.num_experts, self.hidden, self.inter, self.top_k, self.max_tokens, FORMATS[self.fmt], 0,
+                      self.act_alpha, self.act_beta, 0.0 if self.act_clamp is None else self.act_clamp,
+                      0 if self.act_clamp is None else 1, self.shared_inter, FORMATS[self.shared_fmt],
+                      1 if self.post_norm else 0, self.norm_eps, FLAG_DEBUG_H if self.debug_h else 0)
+
+
+def validate(cfg: LayerConfig) -> int:
+    c = cfg.to_c()
+    return lib().moe_config_validate(ctypes.byref(c))
+
+
+def config_workspace_size(cfg: LayerConfig, num_tokens: int) -> int:
+    c = cfg.to_c()
+    n = ctypes.c_size_t()
+    _check("moe_config_workspace_size", lib().moe_config_workspace_size(ctypes.byref(c), num_tokens, ctypes.byref(n)))
+    return n.value
+
+
+def _weights_struct(d: dict | None) -> Weights | None:
+    if d is None:
+        return None
+    return Weights(*[_ptr(d.get(k)) for k in ("w13", "w13_sf", "w13_gs", "w2", "w2_sf", "w2_gs")])
+
+
+class Plan:
+    """A configured layer on the current CUDA device (moe_plan)."""
+
+    def __init__(self, cfg: LayerConfig):
+        self.cfg = cfg
+        self._c = cfg.to_c()
+        h = ctypes.c_void_p()
+        _check("moe_plan", lib().moe_plan(ctypes.byref(self._c), ctypes.byref(h)))
+        self._h = h
+
+    def __del__(self):
+        if getattr(self, "_h", None) and _lib is not None:
+            _lib.moe_plan_destroy(self._h)
+            self._h = None
+
+    def block_m(self, num_tokens: int) -> int:
+        v = ctypes.c_int32()
+        _check("moe_plan_block_m", lib().moe_plan_block_m(self._h, num_tokens, ctypes.byref(v)))
+        return v.value
+
+    def workspace_size(self, num_tokens: int) -> int:
+        n = ctypes.c_size_t()
+        _check("moe_workspace_size", lib().moe_workspace_size(self._h, num_tokens, ctypes.byref(n)))
+        return n.value
+
+    def weight_layout_size(self, which: int) -> int:
+        n = ctypes.c_size_t()
+        _check("moe_weight_layout_size", lib().moe_weight_layout_size(self._h, which, ctypes.byref(n)))
+        return n.value
+
+    def region(self, workspace: torch.Tensor, num_tokens: int, name: str) -> torch.Tensor:
+        """A uint8 view of one workspace region (intermediate results of moe_forward)."""
+        off, n = ctypes.c_size_t(), ctypes.c_size_t()
+        _check("moe_workspace_region",
+               lib().moe_workspace_region(self._h, num_tokens, REGIONS[name], ctypes.byref(off), ctypes.byref(n)))
+        return workspace[off.value: off.value + n.value]
+
+    def alloc_workspace(self, num_tokens: int, device=None) -> torch.Tensor:
+        return torch.zeros(max(self.workspace_size(num_tokens), 1), dtype=torch.uint8,
+                           device=device or torch.cuda.current_device())
+
+    def _alloc_layout(self, ids: dict, device) -> dict:
+        out = {}
+        for key, which in ids.items():
+            n = self.weight_layout_size(which)
+            if n:
+                dt = torch.float32 if key.endswith("_gs") else torch.uint8
+                out[key] = torch.empty(n // (4 if dt == torch.float32 else 1), dtype=dt, device=device)
+        return out
+
+    def transform_weights(self, ckpt: dict, stream=None) -> dict:
+        """Checkpoint-layout routed weights (device tensors) -> kernel-layout tensors."""
+        dev = ckpt["w13"].device
+        dst = self._alloc_layout({"w13": W13, "w13_sf": W13_SF, "w2": W2, "w2_sf": W2_SF,
+                                  "w13_gs": W13_GS, "w2_gs": W2_GS}, dev)
+        s, d = _weights_struct(ckpt), _weights_struct(dst)
+        _check("moe_transform_weights",
+               lib().moe_transform_weights(self._h, ctypes.byref(s), ctypes.byref(d), _stream(stream)))
+        return dst
+
+    def transform_shared_weights(self, ckpt: dict, stream=None) -> dict:
+        dev = ckpt["w13"].device
+        dst = self._alloc_layout({"w13": SHARED_W13, "w13_sf": SHARED_W13_SF, "w2": SHARED_W2,
+                                  "w2_sf": SHARED_W2_SF}, dev)
+        s, d = _weights_struct(ckpt), _weights_struct(dst)
+        _check("moe_transform_shared_weights",
+               lib().moe_transform_shared_weights(self._h, ctypes.byref(s), ctypes.byref(d), _stream(stream)))
+        return dst
+
+    def forward(self, hidden: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, weights: dict,
+                l2_act_scale: torch.Tensor | None = None, shared: dict | None = None,
+                norm_gamma: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """moe_forward: hidden bf16 [T, H] -> out bf16 [T, H]."""
+        T = hidden.shape[0]
+        if out is None:
+            out = torch.empty_like(hidden)
+        if workspace is None:
+            workspace = self.alloc_workspace(T, hidden.device)
+        w = _weights_struct(weights)
+        sh = _weights_struct(shared)
+        _check("moe_forward", lib().moe_forward(
+            self._h, T, _ptr(hidden), _ptr(topk_ids), _ptr(topk_weights), ctypes.byref(w), _ptr(l2_act_scale),
+            ctypes.byref(sh) if sh is not None else None, _ptr(norm_gamma), _ptr(out), _ptr(workspace),
+            workspace.numel(), _stream(stream)))
+        return out
+
+    def last_status(self, workspace: torch.Tensor, stream=None) -> int:
+        v = ctypes.c_int32()
+        _check("moe_last_status", lib().moe_last_status(self._h, _ptr(workspace), _stream(stream), ctypes.byref(v)))
+        return v.value

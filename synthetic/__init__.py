@@ -203,7 +203,7 @@ class Checkpoint:
 # nominal L2-input amax / 2688 for recipe-B NVFP4 checkpoints (set from the
 # oracle's h on sampled rows of these distributions; any positive value is a
 # valid input, it only moves how many L2 input codes saturate)
-NVFP4_A2_NOMINAL = 2.0e-3
+NVFP4_A2_NOMINAL = 2.0e-2
 
 
 def routed_code_checkpoint(shape: MoeShape, seed: int = 0, experts=None) -> Checkpoint:

@@ -1,0 +1,184 @@
+"""Shared helpers of the GPU parity tests: build a seeded case, run it through the
+C ABI (serving_topk_permute_gb300), run the oracle on the same inputs, compare.
+
+Two weight recipes:
+  float  fp32 weights ~ N(0, 1/sqrt(K)) quantised by the oracle's quantiser
+         (reduced sizes; the exact recipe of the workloads)
+  codes  checkpoint bytes drawn directly (synthetic.routed_code_checkpoint) for
+         the experts the sampled tokens touch; every other expert gets random
+         device bytes, which only feed outputs that are not compared
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import synthetic as S
+from oracle import formats as OF
+from oracle import moe as OM
+import serving_topk_permute_gb300 as pkg
+
+# max |gpu - oracle| <= REL * rms(oracle) + ABS
+REL = {"bf16": 2e-2, "mxfp8": 2e-2, "nvfp4": 5e-2}
+ABS = 1e-3
+
+
+def dev():
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def to_dev(a: np.ndarray) -> torch.Tensor:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(dev())
+    return torch.from_numpy(a).to(dev())
+
+
+def bf16_dev(bits: np.ndarray) -> torch.Tensor:
+    return to_dev(bits.astype(np.uint16)).view(torch.bfloat16)
+
+
+@dataclass
+class Case:
+    shape: S.MoeShape
+    x: np.ndarray                    # bf16 bits [T, H]
+    ids: np.ndarray                  # int32 [T, k]
+    w: np.ndarray                    # fp32 [T, k]
+    layer: OM.Layer                  # oracle side (routed / shared checkpoints, a2, gamma)
+    touched: list | None = None      # codes recipe: experts with real weights
+    extra: dict = field(default_factory=dict)
+
+
+def float_case(shape: S.MoeShape, seed: int = 0, ids=None, w=None) -> Case:
+    x = S.hidden_states(shape, seed)
+    if ids is None:
+        ids, w = S.router(shape, seed)
+    w13f, w2f = S.routed_float_weights(shape, seed)
+    routed = OM.quantize_weights(shape.fmt, w13f, w2f)
+    layer = OM.Layer(shape.E, shape.k, routed)
+    if shape.fmt == "nvfp4":
+        layer.a2 = OM.calibrate_a2(layer, x, ids)
+    if shape.shared_I:
+        s13, s2 = S.shared_float_weights(shape, seed)
+        layer.shared = OM.quantize_weights(shape.shared_fmt, s13[None], s2[None])
+    if shape.post_norm:
+        layer.norm_gamma = S.norm_gamma(shape, seed)
+        layer.norm_eps = shape.norm_eps
+    return Case(shape, x, np.asarray(ids, np.int32), np.asarray(w, np.float32), layer)
+
+
+def code_case(shape: S.MoeShape, sample_tokens, seed: int = 0) -> Case:
+    x = S.hidden_states(shape, seed)
+    ids, w = S.router(shape, seed)
+    touched = sorted(set(int(e) for e in ids[sample_tokens].reshape(-1) if e >= 0))
+    ck = S.routed_code_checkpoint(shape, seed, experts=touched)
+    routed = OM.ExpertWeights(ck.fmt, ck.w13, ck.w2, ck.w13_sf, ck.w2_sf, ck.w13_gs, ck.w2_gs)
+    layer = OM.Layer(shape.E, shape.k, routed)
+    if shape.fmt == "nvfp4":
+        layer.a2 = OM.l2_activation_scale(ck.w2_input_scale)
+    if shape.shared_I:
+        sc = S.shared_code_checkpoint(shape, seed)
+        layer.shared = OM.ExpertWeights(sc.fmt, sc.w13, sc.w2, sc.w13_sf, sc.w2_sf)
+    if shape.post_norm:
+        layer.norm_gamma = S.norm_gamma(shape, seed)
+        layer.norm_eps = shape.norm_eps
+    return Case(shape, x, ids, w, layer, touched=touched)
+
+
+def _ckpt_dev(ew: OM.ExpertWeights, touched=None) -> dict:
+    out = {}
+    for key in ("w13", "w13_sf", "w2", "w2_sf", "w13_gs", "w2_gs"):
+        a = getattr(ew, key)
+        if a is None:
+            continue
+        if touched is None or key.endswith("_gs"):
+            out[key] = to_dev(a)
+            continue
+        if a.dtype == np.uint16:
+            t = torch.randint(-2 ** 15, 2 ** 15, a.shape, dtype=torch.int16, device=dev())
+        else:
+            t = torch.randint(0, 256, a.shape, dtype=torch.uint8, device=dev())
+        for e in touched:
+            t[e] = to_dev(a[e])
+        out[key] = t
+    return out
+
+
+def layer_config(case: Case, debug_h=False, max_tokens=None) -> pkg.LayerConfig:
+    s = case.shape
+    act = case.layer.act
+    return pkg.LayerConfig(s.E, s.H, s.I, s.k, max_tokens or max(case.x.shape[0], 1), s.fmt,
+                           act_alpha=act.alpha, act_beta=act.beta, act_clamp=act.clamp,
+                           shared_inter=s.shared_I, shared_fmt=s.shared_fmt, post_norm=s.post_norm,
+                           norm_eps=s.norm_eps, debug_h=debug_h)
+
+
+@dataclass
+class GpuRun:
+    plan: pkg.Plan
+    out: torch.Tensor
+    workspace: torch.Tensor
+    kweights: dict
+    kshared: dict | None
+    inputs: dict
+
+
+def run_gpu(case: Case, debug_h=False, max_tokens=None) -> GpuRun:
+    plan = pkg.Plan(layer_config(case, debug_h, max_tokens))
+    ck = _ckpt_dev(case.layer.routed, case.touched)
+    kw = plan.transform_weights(ck)
+    ks = None
+    if case.layer.shared is not None:
+        ks = plan.transform_shared_weights(_ckpt_dev(case.layer.shared))
+    T = case.x.shape[0]
+    inputs = dict(hidden=bf16_dev(case.x), topk_ids=to_dev(case.ids.astype(np.int32)),
+                  topk_weights=to_dev(case.w.astype(np.float32)))
+    a2 = None
+    if case.shape.fmt == "nvfp4":
+        a2 = torch.tensor([np.float32(case.layer.a2)], dtype=torch.float32, device=dev())
+    gamma = None if case.layer.norm_gamma is None else to_dev(np.asarray(case.layer.norm_gamma, np.float32))
+    ws = plan.alloc_workspace(T)
+    out = plan.forward(inputs["hidden"], inputs["topk_ids"], inputs["topk_weights"], kw, l2_act_scale=a2,
+                       shared=ks, norm_gamma=gamma, workspace=ws)
+    torch.cuda.synchronize()
+    inputs.update(a2=a2, gamma=gamma)
+    return GpuRun(plan, out, ws, kw, ks, inputs)
+
+
+def out_f64(run: GpuRun) -> np.ndarray:
+    return run.out.float().cpu().numpy().astype(np.float64)
+
+
+def oracle_out(case: Case, tokens=None) -> np.ndarray:
+    return OF.bf16_bits_to_f64(OM.forward(case.layer, case.x, case.ids, case.w, tokens=tokens))
+
+
+def assert_close(got: np.ndarray, want: np.ndarray, fmt: str, what=""):
+    rms = float(np.sqrt(np.mean(want ** 2)))
+    tol = REL[fmt] * rms + ABS
+    err = float(np.abs(got - want).max()) if want.size else 0.0
+    assert np.isfinite(got).all(), f"{what}: non-finite GPU output"
+    assert err <= tol, f"{what}: max |gpu - oracle| = {err:.4g} > {tol:.4g} (rms {rms:.4g})"
+    return err, tol
+
+
+def region_i32(run: GpuRun, T: int, name: str) -> np.ndarray:
+    return run.plan.region(run.workspace, T, name).cpu().numpy().view(np.int32)
+
+
+def region_u8(run: GpuRun, T: int, name: str) -> np.ndarray:
+    return run.plan.region(run.workspace, T, name).cpu().numpy()
+
+
+def unpack_act_sf(atoms: np.ndarray, rows: np.ndarray, n_blocks: int, S: int) -> np.ndarray:
+    """Scale bytes [len(rows), n_blocks] from activation scale atoms laid out
+    [row tile][K stage][S][512] with row 32j+i / scale b at byte 16i + 4j + b."""
+    nks = n_blocks // (4 * S)
+    r = rows[:, None].astype(np.int64)
+    kb = np.arange(n_blocks)[None, :]
+    mt, m = r // 128, r % 128
+    ks, s, b = kb // (4 * S), (kb // 4) % S, kb % 4
+    off = ((mt * nks + ks) * S + s) * 512 + (m % 32) * 16 + (m // 32) * 4 + b
+    return atoms[off]

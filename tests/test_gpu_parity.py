@@ -1,0 +1,287 @@
+"""GPU parity of the C-ABI path against the CPU oracle (needs a GB300).
+
+Bit-exact: routing (counts, padded offsets, permutation, inverse), dispatch
+codes and scales, per-token NVFP4 scales, the L2-input codes of the GPU's own
+fp32 h. Within the layer's tolerance (max |gpu - oracle| <= rel * rms + 1e-3,
+rel 2e-2 BF16/MXFP8, 5e-2 NVFP4): every output at reduced sizes spanning
+several tiles with ragged tails, and sampled tokens at the full workload sizes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic as S
+from oracle import formats as OF
+from oracle import moe as OM
+from oracle import routing as OR
+import gpu_case as G
+
+pytestmark = pytest.mark.gpu
+
+W = S.WORKLOADS
+
+REDUCED = {
+    "bf16_toy": W["bf16_toy"],
+    "mxfp8_small": S.shrink(W["mxfp8_small"], T=200, H=512, I=384, E=16, k=4),
+    "mxfp8_h384": S.shrink(W["mxfp8_small"], T=77, H=384, I=256, E=8, k=3),
+    "nvfp4_decode": S.shrink(W["nvfp4_decode"], T=40, H=1024, I=512, E=32, k=8),
+    "mxfp8_prefill_zipf": S.shrink(W["mxfp8_prefill_zipf"], T=512, H=768, I=256, E=32, k=8),
+    "nvfp4_shared_norm": S.shrink(W["nvfp4_shared_norm"], T=130, H=512, I=256, E=16, k=4, shared_I=512),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    import serving_topk_permute_gb300 as pkg
+    pkg.lib()
+
+
+# ----------------------------------------------------------------------------- routing + dispatch, full size
+
+def _ids_only_case(shape):
+    """Full-size inputs; weights are random device bytes (routing / dispatch do not read them)."""
+    return G.code_case(shape, sample_tokens=[], seed=0)
+
+
+@pytest.mark.parametrize("name", S.WORKLOAD_ORDER)
+def test_routing_and_dispatch_bit_exact_full_size(name):
+    shape = W[name]
+    case = _ids_only_case(shape)
+    run = G.run_gpu(case)
+    T, k, E = shape.T, shape.k, shape.E
+    cnt, off, src, inv = OR.permute(case.ids, E, run.plan.block_m(T))
+    assert np.array_equal(G.region_i32(run, T, "counts")[:E], cnt)
+    assert np.array_equal(G.region_i32(run, T, "offsets")[:E + 1], off)
+    M_pad = int(off[-1])
+    assert np.array_equal(G.region_i32(run, T, "src")[:M_pad], src)
+    assert np.array_equal(G.region_i32(run, T, "inv_perm")[:T * k].reshape(T, k), inv)
+    meta = G.region_i32(run, T, "meta")
+    assert meta[0] == M_pad and meta[1] == M_pad // 128
+
+    # dispatch codes: every routed row holds its token's codes
+    d = OM.dispatch_quantize(case.x, shape.fmt)
+    rows = inv.reshape(-1)
+    toks = np.repeat(np.arange(T), k)
+    xq = G.region_u8(run, T, "xq")
+    if shape.fmt == "bf16":
+        got = xq.reshape(-1, shape.H * 2)[rows].view(np.uint16)
+        assert np.array_equal(got, case.x[toks])
+        return
+    row_bytes = shape.H if shape.fmt == "mxfp8" else shape.H // 2
+    got_codes = xq.reshape(-1, row_bytes)[rows]
+    assert np.array_equal(got_codes, d.codes[toks])
+    S_atoms = 1 if shape.fmt == "mxfp8" else 4
+    nblk = shape.H // (32 if shape.fmt == "mxfp8" else 16)
+    got_sf = G.unpack_act_sf(G.region_u8(run, T, "xsf"), rows, nblk, S_atoms)
+    assert np.array_equal(got_sf, d.sf[toks])
+    if shape.fmt == "nvfp4":
+        xs = G.region_u8(run, T, "x_scale").view(np.float32)[:T]
+        assert np.array_equal(xs, d.x_scale)
+    assert run.plan.last_status(run.workspace) == 0
+
+
+# ----------------------------------------------------------------------------- outputs, reduced sizes, every element
+
+@pytest.mark.parametrize("name", list(REDUCED))
+def test_forward_matches_oracle_reduced(name):
+    shape = REDUCED[name]
+    case = G.float_case(shape)
+    run = G.run_gpu(case)
+    G.assert_close(G.out_f64(run), G.oracle_out(case), shape.fmt, name)
+    assert run.plan.last_status(run.workspace) == 0
+
+
+@pytest.mark.parametrize("name", ["mxfp8_small", "nvfp4_decode", "nvfp4_shared_norm", "bf16_toy"])
+def test_l2_input_codes_bit_exact(name):
+    """Apply the oracle's quantiser to the GPU's own fp32 h: codes and scales must match."""
+    shape = REDUCED[name]
+    case = G.float_case(shape)
+    run = G.run_gpu(case, debug_h=True)
+    T = shape.T
+    src = G.region_i32(run, T, "src")
+    M_pad = int(G.region_i32(run, T, "meta")[0])
+    rows = np.nonzero(src[:M_pad] >= 0)[0]
+    h = G.region_u8(run, T, "h_debug").view(np.float32).reshape(-1, shape.I)[rows]
+    assert np.isfinite(h).all()
+    codes, sf = OM.l2_input_codes(h, shape.fmt, case.layer.a2)
+    hq = G.region_u8(run, T, "hq")
+    if shape.fmt == "bf16":
+        got = hq.reshape(-1, shape.I * 2)[rows].view(np.uint16)
+        assert np.array_equal(got, codes)
+        return
+    rb = shape.I if shape.fmt == "mxfp8" else shape.I // 2
+    assert np.array_equal(hq.reshape(-1, rb)[rows], codes)
+    S_atoms = 1 if shape.fmt == "mxfp8" else 4
+    nblk = shape.I // (32 if shape.fmt == "mxfp8" else 16)
+    assert np.array_equal(G.unpack_act_sf(G.region_u8(run, T, "hsf"), rows, nblk, S_atoms), sf)
+    # and h itself is the oracle's h up to fp32 accumulation
+    parts = OM.forward(case.layer, case.x, case.ids, case.w, return_parts=True)[1]
+    want = np.stack([parts["h"][r] for r in rows])
+    scale = np.sqrt(np.mean(want ** 2))
+    assert np.abs(h - want).max() <= 2e-2 * scale + 1e-3
+
+
+# ----------------------------------------------------------------------------- outputs, full size, sampled tokens
+
+@pytest.mark.parametrize("name", ["mxfp8_small", "nvfp4_decode", "mxfp8_prefill_zipf", "nvfp4_shared_norm"])
+def test_forward_matches_oracle_full_size_sampled(name):
+    shape = W[name]
+    T = shape.T
+    sample = sorted(set([0, 1, T // 3, T // 2, T - 2, T - 1]))
+    case = G.code_case(shape, sample)
+    run = G.run_gpu(case)
+    got = G.out_f64(run)[sample]
+    G.assert_close(got, G.oracle_out(case, tokens=sample), shape.fmt, name)
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+def _small_case(fmt="mxfp8", **kw):
+    base = {"bf16": "bf16_toy", "mxfp8": "mxfp8_small", "nvfp4": "nvfp4_decode"}[fmt]
+    shape = S.shrink(W[base], **{"T": 64, "H": 256, "I": 256, "E": 8, "k": 2, **kw})
+    return shape
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4"])
+def test_single_token(fmt):
+    shape = _small_case(fmt, T=1)
+    case = G.float_case(shape)
+    G.assert_close(G.out_f64(G.run_gpu(case)), G.oracle_out(case), fmt, "T=1")
+
+
+def test_masked_slots_and_duplicates():
+    shape = _small_case("mxfp8", T=96, k=3)
+    ids, w = S.router(shape)
+    ids = ids.copy()
+    ids[::3, 1] = -1                 # masked slots
+    ids[1::5, 2] = ids[1::5, 0]      # the same expert twice in one token
+    case = G.float_case(shape, ids=ids, w=w)
+    G.assert_close(G.out_f64(G.run_gpu(case)), G.oracle_out(case), "mxfp8", "masked/dup")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "nvfp4"])
+def test_all_tokens_one_expert(fmt):
+    shape = _small_case(fmt, T=300, k=1)
+    ids = np.full((300, 1), 5, np.int32)
+    w = np.ones((300, 1), np.float32)
+    case = G.float_case(shape, ids=ids, w=w)
+    run = G.run_gpu(case)
+    G.assert_close(G.out_f64(run), G.oracle_out(case), fmt, "one expert")
+    off = G.region_i32(run, 300, "offsets")[:9]
+    assert off.tolist() == [0, 0, 0, 0, 0, 0, 384, 384, 384]
+
+
+def test_bad_expert_id_reports_status_and_is_masked():
+    shape = _small_case("bf16", T=32)
+    ids, w = S.router(shape)
+    bad = ids.copy()
+    bad[3, 0] = shape.E + 5
+    case = G.float_case(shape, ids=bad, w=w)
+    run = G.run_gpu(case)
+    assert run.plan.last_status(run.workspace) == 6
+    masked = bad.copy()
+    masked[3, 0] = -1
+    ref = G.Case(case.shape, case.x, masked, case.w, case.layer)
+    G.assert_close(G.out_f64(run), G.oracle_out(ref), "bf16", "bad id")
+
+
+def test_capacity_and_empty_batch():
+    import serving_topk_permute_gb300 as pkg
+    shape = _small_case("bf16", T=16)
+    case = G.float_case(shape)
+    run = G.run_gpu(case)
+    with pytest.raises(pkg.MoeError) as e:
+        big = torch.zeros((17, shape.H), dtype=torch.bfloat16, device="cuda")
+        run.plan.forward(big, torch.zeros((17, 2), dtype=torch.int32, device="cuda"),
+                         torch.zeros((17, 2), dtype=torch.float32, device="cuda"), run.kweights,
+                         workspace=run.workspace)
+    assert e.value.status == 3
+    empty = torch.zeros((0, shape.H), dtype=torch.bfloat16, device="cuda")
+    out = run.plan.forward(empty, torch.zeros((0, 2), dtype=torch.int32, device="cuda"),
+                           torch.zeros((0, 2), dtype=torch.float32, device="cuda"), run.kweights,
+                           workspace=run.workspace)
+    assert out.shape == (0, shape.H)
+
+
+def test_workspace_too_small():
+    import serving_topk_permute_gb300 as pkg
+    shape = _small_case("bf16", T=16)
+    case = G.float_case(shape)
+    run = G.run_gpu(case)
+    with pytest.raises(pkg.MoeError) as e:
+        run.plan.forward(run.inputs["hidden"], run.inputs["topk_ids"], run.inputs["topk_weights"], run.kweights,
+                         workspace=run.workspace[:1024])
+    assert e.value.status == 4
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_deterministic(fmt):
+    shape = _small_case(fmt, T=150, k=4, E=8)
+    case = G.float_case(shape)
+    a = G.run_gpu(case).out.clone()
+    b = G.run_gpu(case).out.clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("alpha,beta,clamp", [(1.702, 1.0, 7.0), (1.0, 0.0, 0.5), (0.5, -0.25, None)])
+def test_activation_variants(alpha, beta, clamp):
+    shape = _small_case("mxfp8", T=80)
+    case = G.float_case(shape)
+    case.layer.act = OM.Activation(alpha=alpha, beta=beta, clamp=clamp)
+    G.assert_close(G.out_f64(G.run_gpu(case)), G.oracle_out(case), "mxfp8", "activation")
+
+
+# ----------------------------------------------------------------------------- weight layout
+
+def _expected_interleave(w13: np.ndarray, I: int) -> np.ndarray:
+    """Kernel row 256b + 128h + r holds checkpoint row h*I + 128b + r."""
+    E = w13.shape[0]
+    out = np.empty_like(w13)
+    for n in range(2 * I):
+        b, h, r = n // 256, (n % 256) // 128, n % 128
+        out[:, n] = w13[:, h * I + 128 * b + r]
+    return out
+
+
+def _expected_sf_atoms(sf: np.ndarray, N: int, K: int, g: int, interleave: bool, I: int) -> np.ndarray:
+    """Row 32j+i / scale b of 4 at byte 16i + 4j + b of a 512-byte atom (the UTCCP row
+    permutation 128c + 32j + i -> 128c + 4i + j in 32-bit words), atoms [E][N/256][stage][S][2]."""
+    E = sf.shape[0]
+    S_atoms = 1 if g == 32 else 4
+    nkb = K // g
+    nks = nkb // (4 * S_atoms)
+    nt_n = -(-N // 256)
+    out = np.zeros((E, nt_n, nks, S_atoms, 2, 512), np.uint8)
+    for n in range(nt_n * 256):
+        if n >= N:
+            continue
+        row = n
+        if interleave:
+            b, h, r = n // 256, (n % 256) // 128, n % 128
+            row = h * I + 128 * b + r
+        nt, nb, m = n // 256, (n % 256) // 128, n % 128
+        for kb in range(nkb):
+            ks, s, bb = kb // (4 * S_atoms), (kb // 4) % S_atoms, kb % 4
+            out[:, nt, ks, s, nb, (m % 32) * 16 + (m // 32) * 4 + bb] = sf[:, row, kb]
+    return out.reshape(-1)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4"])
+def test_weight_transform_layout(fmt):
+    shape = _small_case(fmt, H=512 if fmt != "mxfp8" else 384, I=256, E=3)
+    case = G.float_case(shape)
+    run = G.run_gpu(case)
+    ew = case.layer.routed
+    kw = {k: v.cpu().numpy() for k, v in run.kweights.items()}
+    w13 = ew.w13.view(np.uint8).reshape(shape.E, 2 * shape.I, -1)
+    assert np.array_equal(kw["w13"], _expected_interleave(w13, shape.I).reshape(-1))
+    assert np.array_equal(kw["w2"], ew.w2.view(np.uint8).reshape(-1))
+    if fmt == "bf16":
+        return
+    g = 32 if fmt == "mxfp8" else 16
+    assert np.array_equal(kw["w13_sf"], _expected_sf_atoms(ew.w13_sf, 2 * shape.I, shape.H, g, True, shape.I))
+    assert np.array_equal(kw["w2_sf"], _expected_sf_atoms(ew.w2_sf, shape.H, shape.I, g, False, shape.I))
+    if fmt == "nvfp4":
+        assert np.array_equal(kw["w13_gs"], ew.w13_gs) and np.array_equal(kw["w2_gs"], ew.w2_gs)
