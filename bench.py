@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Benchmark of the routed-expert MoE layer forward on GB300 (libmoe.so, C ABI).
+
+One step = one moe_forward over one batch of synthetic tokens: routing,
+dispatch quantisation, L1 GEMM (+SwiGLU, requant), L2 GEMM, [shared expert],
+combine [+RMSNorm]. Inputs are resident in HBM when the timed region starts;
+the L2 cache is flushed (a 256 MB write) before every timed step, outside the
+step's own events. Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank runs its own batch of the workload (tokens
+are independent), no collective on the data path; value = all ranks' tokens /
+the slowest rank's time ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic as S  # noqa: E402
+
+METRIC = "MoE layer tokens/s"
+DEFAULT_WORKLOAD = "mxfp8_small"
+FLUSH_BYTES = 256 << 20
+PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# dense tensor throughput relative to bf16 (nominal 2.25 / 4.5 / 13.5 PFLOP/s)
+TENSOR_RATIO = {"bf16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0}
+ELEM_BYTES = {"bf16": 2.0, "mxfp8": 1.0, "nvfp4": 0.5}
+SF_PER_ELEM = {"bf16": 0.0, "mxfp8": 1.0 / 32, "nvfp4": 1.0 / 16}
+# tokens the CPU oracle processes per timed sample (about 10-30 s of host work)
+CPU_SAMPLE_TOKENS = {"bf16_toy": 64, "mxfp8_small": 24, "nvfp4_decode": 3, "mxfp8_prefill_zipf": 12,
+                     "nvfp4_shared_norm": 6}
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def reduce_max(value: float) -> float:
+    """Max over ranks (identity when torch.distributed is not initialised)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own tokens (weak scaling: independent batches)."""
+    return rank
+
+
+# ----------------------------------------------------------------------------- work accounting
+
+def algorithmic_work(shape: S.MoeShape, ids: np.ndarray) -> dict:
+    """Bytes and FLOPs the method itself needs per step and per kernel: weights of the
+    touched experts read once (codes + block scales), activations read once, outputs
+    written once. BLOCK_M padding and staging copies are not counted."""
+    eb, sf = ELEM_BYTES[shape.fmt], SF_PER_ELEM[shape.fmt]
+    H, I, T, k = shape.H, shape.I, shape.T, shape.k
+    routed = ids[ids >= 0]
+    R = routed.size
+    touched = len(np.unique(routed))
+    w13 = touched * 2 * I * H * (eb + sf)
+    w2 = touched * H * I * (eb + sf)
+    gs = 8 * touched if shape.fmt == "nvfp4" else 0
+    x_in = R * H * (eb + sf)           # dispatched rows read by L1
+    h_bytes = R * I * (eb + sf)         # L2 input written by L1, read by L2
+    y_bytes = R * H * 2                 # per-row bf16 output of L2
+    per_kernel = {
+        "l1": {"bytes": w13 + x_in + h_bytes, "flops": 2.0 * R * 2 * I * H, "fmt": shape.fmt},
+        "l2": {"bytes": w2 + h_bytes + y_bytes, "flops": 2.0 * R * H * I, "fmt": shape.fmt},
+        "dispatch": {"bytes": T * H * 2 + x_in, "flops": 0.0, "fmt": shape.fmt},
+        "combine": {"bytes": y_bytes + T * H * 2, "flops": 0.0, "fmt": shape.fmt},
+        "route": {"bytes": R * 4 * 3, "flops": 0.0, "fmt": shape.fmt},
+    }
+    flops = 2.0 * R * 3 * I * H
+    nbytes = w13 + w2 + gs + T * H * 2 + T * H * 2
+    if shape.shared_I:
+        Is, se, ss = shape.shared_I, ELEM_BYTES[shape.shared_fmt], SF_PER_ELEM[shape.shared_fmt]
+        sw = 3 * Is * H * (se + ss)
+        flops += 2.0 * T * 3 * Is * H
+        nbytes += sw
+        per_kernel["shared_l1"] = {"bytes": 2 * Is * H * (se + ss) + T * H * (se + ss) + T * Is * (se + ss),
+                                   "flops": 2.0 * T * 2 * Is * H, "fmt": shape.shared_fmt}
+        per_kernel["shared_l2"] = {"bytes": Is * H * (se + ss) + T * Is * (se + ss) + T * H * 2,
+                                   "flops": 2.0 * T * Is * H, "fmt": shape.shared_fmt}
+    return {"flops": flops, "bytes": nbytes, "touched_experts": touched, "per_kernel": per_kernel}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAK_FALLBACK), "fallback"
+
+
+def roofline(kernel: str, work: dict, avg_ms: float, peaks: dict, source: str, sustained: bool) -> dict:
+    w = work["per_kernel"][kernel]
+    hbm = float(peaks.get("hbm_gbs", PEAK_FALLBACK["hbm_gbs"]))
+    bf16 = float(peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops",
+                           peaks.get("bf16_tflops", PEAK_FALLBACK["bf16_tflops"])))
+    tensor = bf16 * TENSOR_RATIO[w["fmt"]]
+    t_mem = w["bytes"] / (hbm * 1e9)
+    t_tc = w["flops"] / (tensor * 1e12) if w["flops"] else 0.0
+    sec = avg_ms / 1e3
+    if t_mem >= t_tc:
+        achieved = w["bytes"] / sec / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": None, "kernel": kernel,
+                "peak_source": f"{source} hbm_gbs", "algorithmic_bytes": int(w["bytes"])}
+    achieved = w["flops"] / sec / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(tensor, 1), "unit": "TFLOP/s",
+            "frac": round(achieved / tensor, 4), "traffic": None, "kernel": kernel,
+            "peak_source": f"{source} {'bf16_tflops_sustained' if sustained else 'bf16_tflops'} x "
+                           f"{TENSOR_RATIO[w['fmt']]:g} ({w['fmt']} nominal ratio)",
+            "algorithmic_flops": w["flops"]}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
+
+def oracle_sample(shape: S.MoeShape, seed: int, n_tokens: int):
+    """Time the CPU oracle on the first n_tokens tokens of the workload (recipe-B weights of the experts
+    those tokens touch). Returns (seconds, tokens, cores)."""
+    from oracle import moe as OM
+    x = S.hidden_states(shape, seed)
+    ids, w = S.router(shape, seed)
+    toks = list(range(min(n_tokens, shape.T)))
+    touched = sorted(set(int(e) for e in ids[toks].reshape(-1)))
+    ck = S.routed_code_checkpoint(shape, seed, experts=touched)
+    layer = OM.Layer(shape.E, shape.k, OM.ExpertWeights(ck.fmt, ck.w13, ck.w2, ck.w13_sf, ck.w2_sf, ck.w13_gs,
+                                                         ck.w2_gs))
+    if shape.fmt == "nvfp4":
+        layer.a2 = OM.l2_activation_scale(ck.w2_input_scale)
+    if shape.shared_I:
+        sc = S.shared_code_checkpoint(shape, seed)
+        layer.shared = OM.ExpertWeights(sc.fmt, sc.w13, sc.w2, sc.w13_sf, sc.w2_sf)
+    if shape.post_norm:
+        layer.norm_gamma = S.norm_gamma(shape, seed)
+        layer.norm_eps = shape.norm_eps
+    t0 = time.perf_counter()
+    OM.forward(layer, x, ids, w, tokens=toks)
+    dt = time.perf_counter() - t0
+    return dt, len(toks), blas_threads()
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def run_reference(args, shape: S.MoeShape):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    n_tok = CPU_SAMPLE_TOKENS[shape.name]
+    if args.warmup > 0:
+        oracle_sample(shape, 0, 1)
+    total_s, total_tok, cores = 0.0, 0, 1
+    for i in range(args.steps):
+        dt, nt, cores = oracle_sample(shape, 0, n_tok)
+        total_s += dt
+        total_tok += nt
+    value = total_tok / total_s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(shape, world),
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {n_tok} tokens of {shape.name} per step (NumPy fp64 oracle)"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(shape: S.MoeShape, world: int) -> dict:
+    return {"workload": shape.name, "T": shape.T, "H": shape.H, "I": shape.I, "E": shape.E, "top_k": shape.k,
+            "format": shape.fmt, "shared_I": shape.shared_I, "shared_format": shape.shared_fmt if shape.shared_I
+            else None, "post_norm": shape.post_norm, "global_batch": shape.T * world,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "flushed before every timed step (256 MB write)"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, shape: S.MoeShape):
+    import torch
+    import torch.distributed as dist
+
+    import serving_topk_permute_gb300 as pkg
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    seed = rank_seed(rank)
+
+    # inputs (host, seeded) and weights (device, seeded)
+    x = S.hidden_states(shape, seed)
+    ids, w = S.router(shape, seed)
+    T = shape.T
+    plan = pkg.Plan(pkg.LayerConfig(shape.E, shape.H, shape.I, shape.k, T, shape.fmt, shared_inter=shape.shared_I,
+                                    shared_fmt=shape.shared_fmt, post_norm=shape.post_norm,
+                                    norm_eps=shape.norm_eps))
+    ck = S.torch_code_checkpoint(shape, seed, dev)
+    kw = plan.transform_weights({k: v for k, v in ck.items() if k != "w2_input_scale"})
+    ks = plan.transform_shared_weights(S.torch_code_checkpoint(shape, seed, dev, shared=True)) \
+        if shape.shared_I else None
+    # NVFP4: one L2 input scale for all experts, the max of the per-expert input scales
+    a2 = ck["w2_input_scale"].max().reshape(1).to(torch.float32) if shape.fmt == "nvfp4" else None
+    del ck
+    gamma = torch.from_numpy(S.norm_gamma(shape, seed)).to(dev) if shape.post_norm else None
+    hidden = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    tid = torch.from_numpy(ids).to(dev)
+    tw = torch.from_numpy(w).to(dev)
+    out = torch.empty_like(hidden)
+    ws = plan.alloc_workspace(T, dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def step():
+        plan.forward(hidden, tid, tw, kw, l2_act_scale=a2, shared=ks, norm_gamma=gamma, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = plan.last_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {pkg.error_string(status)}")
+
+    # ---- device-resident timed region: K replays of a CUDA graph of one forward
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    kernels_per_step = 5 + (2 if shape.shared_I else 0)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_busy = time.perf_counter()
+    while time.perf_counter() - t_busy < 1.0:          # keep the GPU loaded while the sampler starts
+        for _ in range(20):
+            graph.replay()
+        torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record()
+        graph.replay()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = reduce_max(sum(step_ms))
+    value = world * T * args.steps / (total_ms / 1e3)
+
+    # ---- per-kernel times (library events around each launch, same stream, L2 flushed before each step)
+    plan.enable_timing(True)
+    ktimes = {}
+    for i in range(min(args.steps, 200)):
+        flush.fill_(i & 0xFF)
+        step()
+        for k_, v in plan.kernel_times().items():
+            ktimes.setdefault(k_, []).append(v)
+    plan.enable_timing(False)
+
+    # ---- end to end: pinned host inputs -> device -> forward -> host output, every step
+    h_hidden = torch.from_numpy(x.view(np.int16)).pin_memory()
+    h_ids = torch.from_numpy(ids).pin_memory()
+    h_w = torch.from_numpy(w).pin_memory()
+    h_out = torch.empty((T, shape.H), dtype=torch.int16).pin_memory()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e2e_ev[i][0].record()
+        hidden.view(torch.int16).copy_(h_hidden, non_blocking=True)
+        tid.copy_(h_ids, non_blocking=True)
+        tw.copy_(h_w, non_blocking=True)
+        step()
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+        e2e_ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev))
+    e2e_value = world * T * args.steps / (e2e_ms / 1e3)
+    h2d = h_hidden.numel() * 2 + h_ids.numel() * 4 + h_w.numel() * 4
+    d2h = h_out.numel() * 2
+    if plan.last_status(ws) != 0:
+        raise RuntimeError("device status after timing")
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    work = algorithmic_work(shape, ids)
+    avg_k = {k_: statistics.mean(v) for k_, v in ktimes.items() if v and max(v) > 0}
+    dominant = max(avg_k, key=avg_k.get)
+    peaks, source = load_peaks()
+    rl = roofline(dominant, work, avg_k[dominant], peaks, source, sustained=False)
+    rl["kernel_ms"] = {k_: round(v, 4) for k_, v in avg_k.items()}
+    sec = sum(step_ms) / 1e3 / args.steps
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n_tok = CPU_SAMPLE_TOKENS[shape.name]
+        dt, nt, cores = oracle_sample(shape, 0, n_tok)
+        cpu = {"value": round(nt / dt, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"first {nt} tokens of {shape.name} (NumPy fp64 oracle, {dt:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sum(step_ms) / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": shape.fmt if shape.fmt != "bf16" else "bf16",
+        "data": "synthetic (seeded activations and routing; checkpoint bytes drawn on the device)",
+        "config": workload_config(shape, world),
+        "roofline": rl,
+        "layer": {"tflops": round(work["flops"] / sec / 1e12, 2), "hbm_gbs": round(work["bytes"] / sec / 1e9, 1),
+                  "algorithmic_flops": work["flops"], "algorithmic_bytes": int(work["bytes"]),
+                  "touched_experts": work["touched_experts"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": kernels_per_step * args.steps,
+        "timing": "value: CUDA-graph replays of one moe_forward, events per step; e2e: plain C-ABI calls",
+        "clocks": clk,
+        "wall_s": round(wall, 3),
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=S.WORKLOAD_ORDER, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    shape = S.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, shape)
+    return run_ours(args, shape)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -247,6 +247,28 @@ int moe_last_status(moe_plan_t plan, void* workspace, void* stream, int32_t* sta
 int moe_workspace_region(moe_plan_t plan, int32_t num_tokens, int32_t which,
                          size_t* offset, size_t* bytes);
 
+/* ---------------------------------------------------------------- measurement */
+
+#define MOE_KERNEL_ROUTE      0
+#define MOE_KERNEL_DISPATCH   1
+#define MOE_KERNEL_L1         2
+#define MOE_KERNEL_L2         3
+#define MOE_KERNEL_SHARED_L1  4
+#define MOE_KERNEL_SHARED_L2  5
+#define MOE_KERNEL_COMBINE    6
+#define MOE_NUM_KERNELS       7
+
+/*
+ * Per-launch timing. With enable = 1 the plan creates CUDA events and every
+ * later moe_forward records one before and one after each of its kernel
+ * launches on the call's stream (enable = 0 destroys them).
+ * moe_plan_kernel_times waits for the last forward's final event and writes
+ * the elapsed milliseconds of each launch to ms[MOE_KERNEL_*] (0 for a kernel
+ * that did not run); count must be >= MOE_NUM_KERNELS.
+ */
+int moe_plan_enable_timing(moe_plan_t plan, int32_t enable);
+int moe_plan_kernel_times(moe_plan_t plan, float* ms, int32_t count);
+
 /* Static string for a status code. */
 const char* moe_error_string(int32_t status);
 

@@ -161,7 +161,28 @@ struct moe_plan_s {
     int device;
     int num_sms;
     unsigned long long timeout_ns;
+    bool timing = false;
+    cudaEvent_t ev[2 * MOE_NUM_KERNELS] = {};
+    bool ran[MOE_NUM_KERNELS] = {};
 };
+
+namespace {
+// brackets one kernel launch with the plan's timing events (when enabled)
+struct KernelTimer {
+    moe_plan_s* p;
+    int id;
+    cudaStream_t st;
+    KernelTimer(moe_plan_s* p_, int id_, cudaStream_t st_) : p(p_), id(id_), st(st_) {
+        if (p->timing) {
+            cudaEventRecord(p->ev[2 * id], st);
+            p->ran[id] = true;
+        }
+    }
+    ~KernelTimer() {
+        if (p->timing) cudaEventRecord(p->ev[2 * id + 1], st);
+    }
+};
+}  // namespace
 
 #define CUDA_TRY(x)                              \
     do {                                         \
@@ -198,7 +219,31 @@ int moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     return MOE_OK;
 }
 
+int moe_plan_enable_timing(moe_plan_t plan, int32_t enable) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    if (enable && !plan->timing) {
+        for (auto& e : plan->ev) CUDA_TRY(cudaEventCreate(&e));
+        plan->timing = true;
+    } else if (!enable && plan->timing) {
+        for (auto& e : plan->ev) cudaEventDestroy(e);
+        plan->timing = false;
+    }
+    return MOE_OK;
+}
+
+int moe_plan_kernel_times(moe_plan_t plan, float* ms, int32_t count) {
+    if (!plan || !ms || count < MOE_NUM_KERNELS || !plan->timing) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < MOE_NUM_KERNELS; ++i) {
+        ms[i] = 0.0f;
+        if (!plan->ran[i]) continue;
+        CUDA_TRY(cudaEventSynchronize(plan->ev[2 * i + 1]));
+        CUDA_TRY(cudaEventElapsedTime(&ms[i], plan->ev[2 * i], plan->ev[2 * i + 1]));
+    }
+    return MOE_OK;
+}
+
 int moe_plan_destroy(moe_plan_t plan) {
+    if (plan) moe_plan_enable_timing(plan, 0);
     delete plan;
     return MOE_OK;
 }
@@ -301,7 +346,7 @@ int moe_transform_shared_weights(moe_plan_t plan, const moe_weights_t* src, moe_
 }
 
 // one expert MLP pass (L1 then L2) over row tiles of the given A buffers
-static int run_mlp(const moe_plan_s* p, int fmt, int E, int I, int H, const void* xq, const uint8_t* xsf, int64_t rows,
+static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, const void* xq, const uint8_t* xsf, int64_t rows,
                    const moe_weights_t* w, const int* m_tiles_dev, int m_tiles_host, int64_t m_tiles_max,
                    const int* tile_expert, const int* src, int m_valid, const float* x_scale, const float* a2,
                    uint8_t* hq, uint8_t* hsf, float* h_debug, __nv_bfloat16* y, int* err, bool activation,
@@ -338,7 +383,10 @@ static int run_mlp(const moe_plan_s* p, int fmt, int E, int I, int H, const void
     g.h_nks = (int)fmt_k_stages(fmt, I);
     g.h_debug = h_debug;
     const int grid1 = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, m_tiles_max * g.n_tiles));
-    CUDA_TRY(launch_gemm(fmt, true, ta, tb, g, grid1, st));
+    {
+        KernelTimer kt(p, kid1, st);
+        CUDA_TRY(launch_gemm(fmt, true, ta, tb, g, grid1, st));
+    }
     // L2: h [rows, I] x w2[e]^T -> y [rows, H]
     if (!map_2d(&ta, hq, fmt_row_bytes(fmt, I), rows, BM)) return MOE_ERR_CUDA;
     if (!map_3d(&tb, w->w2, fmt_row_bytes(fmt, I), H, E)) return MOE_ERR_CUDA;
@@ -351,7 +399,10 @@ static int run_mlp(const moe_plan_s* p, int fmt, int E, int I, int H, const void
     g.y = y;
     g.ldy = H;
     const int grid2 = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, m_tiles_max * g.n_tiles));
-    CUDA_TRY(launch_gemm(fmt, false, ta, tb, g, grid2, st));
+    {
+        KernelTimer kt(p, kid1 + 1, st);
+        CUDA_TRY(launch_gemm(fmt, false, ta, tb, g, grid2, st));
+    }
     return MOE_OK;
 }
 
@@ -382,9 +433,13 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
     int* err = (int*)R(R_ERR);
     int* meta = (int*)R(R_META);
     CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int), st));  // the status reflects this call only
+    for (bool& r : plan->ran) r = false;
 
-    CUDA_TRY(launch_route(topk_ids, T, d.k, d.E, (int*)R(R_CNT), (int*)R(R_OFF), (int*)R(R_SRC), (int*)R(R_INV),
+    {
+        KernelTimer kt(plan, MOE_KERNEL_ROUTE, st);
+        CUDA_TRY(launch_route(topk_ids, T, d.k, d.E, (int*)R(R_CNT), (int*)R(R_OFF), (int*)R(R_SRC), (int*)R(R_INV),
                           (int*)R(R_TILE_EXPERT), meta, err, st));
+    }
     DispatchArgs da{};
     da.x = (const uint16_t*)hidden;
     da.T = T;
@@ -398,16 +453,19 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
     da.shared_fmt = d.Is > 0 ? d.sfmt : -1;
     da.sxq = R(R_SXQ);
     da.sxsf = R(R_SXSF);
-    CUDA_TRY(launch_dispatch(da, st));
+    {
+        KernelTimer kt(plan, MOE_KERNEL_DISPATCH, st);
+        CUDA_TRY(launch_dispatch(da, st));
+    }
 
-    int rc = run_mlp(plan, d.fmt, d.E, d.I, d.H, R(R_XQ), R(R_XSF), L.m_pad_max, weights, meta + 1, 0, L.m_tiles_max,
+    int rc = run_mlp(plan, MOE_KERNEL_L1, d.fmt, d.E, d.I, d.H, R(R_XQ), R(R_XSF), L.m_pad_max, weights, meta + 1, 0, L.m_tiles_max,
                      (const int*)R(R_TILE_EXPERT), (const int*)R(R_SRC), 0, (const float*)R(R_XSCALE), l2_act_scale,
                      R(R_HQ), R(R_HSF), (c.flags & MOE_FLAG_DEBUG_H) ? (float*)R(R_HDBG) : nullptr,
                      (__nv_bfloat16*)R(R_Y), err, true, st);
     if (rc != MOE_OK) return rc;
     if (d.Is > 0) {
         const int tiles = (int)(L.t_pad / BM);
-        rc = run_mlp(plan, d.sfmt, 1, d.Is, d.H, R(R_SXQ), R(R_SXSF), L.t_pad, shared, nullptr, tiles, tiles, nullptr,
+        rc = run_mlp(plan, MOE_KERNEL_SHARED_L1, d.sfmt, 1, d.Is, d.H, R(R_SXQ), R(R_SXSF), L.t_pad, shared, nullptr, tiles, tiles, nullptr,
                      nullptr, T, nullptr, nullptr, R(R_SHQ), R(R_SHSF), nullptr, (__nv_bfloat16*)R(R_SY), err, false,
                      st);
         if (rc != MOE_OK) return rc;
@@ -423,7 +481,10 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
     ca.gamma = c.post_norm ? norm_gamma : nullptr;
     ca.eps = c.norm_eps;
     ca.out = (__nv_bfloat16*)out;
-    CUDA_TRY(launch_combine(ca, st));
+    {
+        KernelTimer kt(plan, MOE_KERNEL_COMBINE, st);
+        CUDA_TRY(launch_combine(ca, st));
+    }
     return MOE_OK;
 }
 

@@ -24,6 +24,7 @@ W13, W13_SF, W2, W2_SF, SHARED_W13, SHARED_W13_SF, SHARED_W2, SHARED_W2_SF, W13_
 REGIONS = {"counts": 0, "offsets": 1, "src": 2, "inv_perm": 3, "xq": 4, "xsf": 5, "x_scale": 6, "hq": 7,
            "hsf": 8, "h_debug": 9, "y": 10, "meta": 11, "shared_y": 12}
 FLAG_DEBUG_H = 1
+KERNELS = ["route", "dispatch", "l1", "l2", "shared_l1", "shared_l2", "combine"]
 
 
 class MoeError(RuntimeError):
@@ -71,6 +72,8 @@ def lib() -> ctypes.CDLL:
             "moe_forward": [P, I32, P, P, P, P, P, P, P, P, P, SZ, P],
             "moe_last_status": [P, P, P, P],
             "moe_workspace_region": [P, I32, I32, P, P],
+            "moe_plan_enable_timing": [P, I32],
+            "moe_plan_kernel_times": [P, P, I32],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -234,6 +237,15 @@ class Plan:
             ctypes.byref(sh) if sh is not None else None, _ptr(norm_gamma), _ptr(out), _ptr(workspace),
             workspace.numel(), _stream(stream)))
         return out
+
+    def enable_timing(self, enable: bool = True):
+        _check("moe_plan_enable_timing", lib().moe_plan_enable_timing(self._h, 1 if enable else 0))
+
+    def kernel_times(self) -> dict:
+        """Milliseconds of each kernel launch of the last forward (waits for it)."""
+        arr = (ctypes.c_float * len(KERNELS))()
+        _check("moe_plan_kernel_times", lib().moe_plan_kernel_times(self._h, arr, len(KERNELS)))
+        return dict(zip(KERNELS, list(arr)))
 
     def last_status(self, workspace: torch.Tensor, stream=None) -> int:
         v = ctypes.c_int32()

@@ -252,3 +252,43 @@ def shared_code_checkpoint(shape: MoeShape, seed: int = 0) -> Checkpoint:
     w13, w13_sf = mxfp8_codes(2 * S, H, seed, _S_WS13)
     w2, w2_sf = mxfp8_codes(H, S, seed, _S_WS2)
     return Checkpoint(FMT_MXFP8, w13[None], w2[None], w13_sf[None], w2_sf[None])
+
+
+# ----------------------------------------------------------------------------- recipe B drawn on a device
+#
+# The same byte ranges as ``mxfp8_codes`` / ``nvfp4_codes``, drawn with a seeded
+# torch generator on the device (the benchmark's full-size weights: 11 GB of
+# codes are drawn in milliseconds there). Values differ from the host draw;
+# the distribution is the same.
+
+def torch_code_checkpoint(shape: MoeShape, seed: int, device, shared: bool = False) -> dict:
+    """Checkpoint-layout tensors (routed, or the shared expert with E = 1) on `device`."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1000 + (7 if shared else 3))
+    E = 1 if shared else shape.E
+    I = shape.shared_I if shared else shape.I
+    fmt = shape.shared_fmt if shared else shape.fmt
+    H = shape.H
+
+    def ri(lo, hi, size, dtype=torch.uint8):
+        return torch.randint(lo, hi, size, generator=g, device=device, dtype=torch.int32).to(dtype)
+
+    out = {}
+    for key, rows, K in (("w13", 2 * I, H), ("w2", H, I)):
+        if fmt == FMT_BF16:
+            w = torch.randn((E, rows, K), generator=g, device=device) * (1.0 / math.sqrt(K))
+            out[key] = w.to(torch.bfloat16).view(torch.int16)
+        elif fmt == FMT_MXFP8:
+            centre = 127 + int(round(-math.log2(96.0) - 0.5 * math.log2(K)))
+            out[key] = ri(0x30, 0x7F, (E, rows, K)) | (ri(0, 2, (E, rows, K)) << 7)
+            out[key + "_sf"] = ri(centre - 1, centre + 2, (E, rows, K // 32))
+        else:
+            out[key] = ri(0, 256, (E, rows, K // 2))
+            out[key + "_sf"] = ri(0x38, 0x59, (E, rows, K // 16))
+            u = torch.rand((E,), generator=g, device=device) * 0.45 + 0.8
+            out[key + "_gs"] = (u * (1.0 / (12.0 * math.sqrt(K)))).to(torch.float32)
+    if fmt == FMT_NVFP4 and not shared:
+        out["w2_input_scale"] = (torch.rand((E,), generator=g, device=device) * 0.2 + 0.8) * NVFP4_A2_NOMINAL
+    return out

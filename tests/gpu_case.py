@@ -152,7 +152,13 @@ def out_f64(run: GpuRun) -> np.ndarray:
 
 
 def oracle_out(case: Case, tokens=None) -> np.ndarray:
-    return OF.bf16_bits_to_f64(OM.forward(case.layer, case.x, case.ids, case.w, tokens=tokens))
+    """The oracle's output before its final bf16 rounding (fp64).
+
+    The GPU's bf16 output is compared with this exact value: two correct
+    results that differ by 1e-4 relative before the final rounding can land on
+    neighbouring bf16 values, and one bf16 step at |z| > 2.56 rms is already
+    more than 2e-2 rms."""
+    return OM.forward(case.layer, case.x, case.ids, case.w, tokens=tokens, return_parts=True)[1]["z"]
 
 
 def assert_close(got: np.ndarray, want: np.ndarray, fmt: str, what=""):

@@ -1,10 +1,13 @@
 """GPU parity of the C-ABI path against the CPU oracle (needs a GB300).
 
 Bit-exact: routing (counts, padded offsets, permutation, inverse), dispatch
-codes and scales, per-token NVFP4 scales, the L2-input codes of the GPU's own
-fp32 h. Within the layer's tolerance (max |gpu - oracle| <= rel * rms + 1e-3,
-rel 2e-2 BF16/MXFP8, 5e-2 NVFP4): every output at reduced sizes spanning
-several tiles with ragged tails, and sampled tokens at the full workload sizes.
+codes and scales, per-token NVFP4 scales, the weight layouts. The L2-input
+codes equal the oracle's codes of the oracle's h except where the oracle's
+value is within accumulation noise of a rounding midpoint. Within the layer's
+tolerance (max |gpu - oracle| <= rel * rms + 1e-3, rel 2e-2 BF16/MXFP8, 5e-2
+NVFP4; the oracle's value taken before its final bf16 rounding): every output
+at reduced sizes spanning several tiles with ragged tails, and sampled tokens
+at the full workload sizes. Every expected value comes from the oracle.
 """
 import numpy as np
 import pytest
@@ -93,34 +96,74 @@ def test_forward_matches_oracle_reduced(name):
     assert run.plan.last_status(run.workspace) == 0
 
 
+def _near_midpoint(v, a, b, rel):
+    """v lies within rel of the midpoint of the two neighbouring grid values a, b."""
+    mid = (a + b) / 2
+    return np.abs(v - mid) <= rel * np.maximum(np.abs(v), 1e-30)
+
+
 @pytest.mark.parametrize("name", ["mxfp8_small", "nvfp4_decode", "nvfp4_shared_norm", "bf16_toy"])
-def test_l2_input_codes_bit_exact(name):
-    """Apply the oracle's quantiser to the GPU's own fp32 h: codes and scales must match."""
+def test_l2_input_matches_oracle(name):
+    """The GPU's fp32 h against the oracle's h, and the GPU's L2-input codes against the
+    oracle's codes of its own h: equal except where the oracle's value sits within
+    fp32 accumulation noise of a rounding midpoint (then either neighbour is correct)."""
     shape = REDUCED[name]
     case = G.float_case(shape)
     run = G.run_gpu(case, debug_h=True)
-    T = shape.T
+    T, I = shape.T, shape.I
     src = G.region_i32(run, T, "src")
     M_pad = int(G.region_i32(run, T, "meta")[0])
     rows = np.nonzero(src[:M_pad] >= 0)[0]
-    h = G.region_u8(run, T, "h_debug").view(np.float32).reshape(-1, shape.I)[rows]
-    assert np.isfinite(h).all()
-    codes, sf = OM.l2_input_codes(h, shape.fmt, case.layer.a2)
+    parts = OM.forward(case.layer, case.x, case.ids, case.w, return_parts=True)[1]
+    h_or = np.stack([parts["h"][r] for r in rows])                      # rows are the oracle's rows too
+    h_gpu = G.region_u8(run, T, "h_debug").view(np.float32).reshape(-1, I)[rows].astype(np.float64)
+    rel_err = np.abs(h_gpu - h_or).max() / np.abs(h_or).max()
+    assert rel_err < 1e-4, rel_err
+    DELTA = 1e-4                                                         # allowed distance to a midpoint
+
+    codes, sf = OM.l2_input_codes(h_or.astype(np.float32), shape.fmt, case.layer.a2)
     hq = G.region_u8(run, T, "hq")
     if shape.fmt == "bf16":
-        got = hq.reshape(-1, shape.I * 2)[rows].view(np.uint16)
-        assert np.array_equal(got, codes)
+        got = hq.reshape(-1, I * 2)[rows].view(np.uint16)
+        diff = got != codes
+        a, b = OF.bf16_bits_to_f64(got[diff]), OF.bf16_bits_to_f64(codes[diff])
+        assert np.all(_near_midpoint(h_or[diff], a, b, DELTA))
+        assert diff.mean() < 1e-3
         return
-    rb = shape.I if shape.fmt == "mxfp8" else shape.I // 2
-    assert np.array_equal(hq.reshape(-1, rb)[rows], codes)
-    S_atoms = 1 if shape.fmt == "mxfp8" else 4
-    nblk = shape.I // (32 if shape.fmt == "mxfp8" else 16)
-    assert np.array_equal(G.unpack_act_sf(G.region_u8(run, T, "hsf"), rows, nblk, S_atoms), sf)
-    # and h itself is the oracle's h up to fp32 accumulation
-    parts = OM.forward(case.layer, case.x, case.ids, case.w, return_parts=True)[1]
-    want = np.stack([parts["h"][r] for r in rows])
-    scale = np.sqrt(np.mean(want ** 2))
-    assert np.abs(h - want).max() <= 2e-2 * scale + 1e-3
+    fmt = shape.fmt
+    rb = I if fmt == "mxfp8" else I // 2
+    got_codes = hq.reshape(-1, rb)[rows]
+    S_atoms, g = (1, 32) if fmt == "mxfp8" else (4, 16)
+    got_sf = G.unpack_act_sf(G.region_u8(run, T, "hsf"), rows, I // g, S_atoms)
+    # block scales: a differing scale byte needs the block's amax at a decision boundary
+    amax = np.abs(h_or.astype(np.float32).astype(np.float64)).reshape(len(rows), -1, g).max(-1)
+    sf_diff = got_sf != sf
+    if fmt == "mxfp8":
+        e = sf[sf_diff].astype(np.int64) - 127
+        bound = np.ldexp(448.0, np.minimum(e, got_sf[sf_diff].astype(np.int64) - 127))
+        assert np.all(np.abs(amax[sf_diff] - bound) <= DELTA * bound)
+        deq_or = OF.mxfp8_dequantize(codes, sf)
+        deq_gpu = OF.mxfp8_dequantize(got_codes, got_sf)
+        scale = OF.UE8M0_TABLE[sf].repeat(g, axis=1)
+        step = scale * 2.0 ** (np.floor(np.log2(np.maximum(np.abs(h_or) / scale, 2.0 ** -6))) - 3)
+    else:
+        a2 = np.float32(case.layer.a2)
+        ratio = amax / (float(a2) * 6.0)
+        assert np.all(_near_midpoint(ratio[sf_diff], OF.E4M3_TABLE[sf[sf_diff]], OF.E4M3_TABLE[got_sf[sf_diff]],
+                                     DELTA) | (sf[sf_diff] == got_sf[sf_diff]))
+        deq_or = OF.nvfp4_dequantize(codes, sf, a2)
+        deq_gpu = OF.nvfp4_dequantize(got_codes, got_sf, a2)
+        eff = (OF.E4M3_TABLE[sf] * float(a2)).repeat(g, axis=1)
+        q = np.abs(h_or) / np.maximum(eff, 1e-30)
+        step = eff * np.where(q < 2, 0.5, np.where(q < 4, 1.0, 2.0))
+    assert sf_diff.mean() < 1e-3, sf_diff.mean()
+    same_block = ~np.repeat(sf_diff, g, axis=1)
+    dv = deq_gpu != deq_or
+    bad = dv & same_block
+    # a differing value in a block with the same scale is the other neighbour of a midpoint
+    assert np.all(np.abs(deq_gpu[bad] - deq_or[bad]) <= step[bad] * (1 + 1e-9))
+    assert np.all(_near_midpoint(h_or[bad], deq_gpu[bad], deq_or[bad], DELTA))
+    assert bad.mean() < 1e-3, bad.mean()
 
 
 # ----------------------------------------------------------------------------- outputs, full size, sampled tokens
