@@ -161,12 +161,26 @@ def oracle_out(case: Case, tokens=None) -> np.ndarray:
     return OM.forward(case.layer, case.x, case.ids, case.w, tokens=tokens, return_parts=True)[1]["z"]
 
 
+def half_ulp_bf16(z: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 values around |z| (8 significant bits)."""
+    e = np.floor(np.log2(np.maximum(np.abs(z), 2.0 ** -126)))
+    return np.ldexp(1.0, (e - 8).astype(np.int64))
+
+
 def assert_close(got: np.ndarray, want: np.ndarray, fmt: str, what=""):
-    rms = float(np.sqrt(np.mean(want ** 2)))
+    """max |gpu - oracle| <= REL * rms(oracle) + ABS, for the value before the final bf16 rounding.
+
+    `want` is the oracle's exact (fp64) output; the GPU's output is bf16, whose own
+    rounding (at most half a bf16 step of the output, which the oracle's bf16 result
+    carries too) is allowed on top: at |z| > 5 rms half a step alone exceeds 2e-2 rms."""
+    rms = float(np.sqrt(np.mean(want ** 2))) if want.size else 0.0
     tol = REL[fmt] * rms + ABS
-    err = float(np.abs(got - want).max()) if want.size else 0.0
     assert np.isfinite(got).all(), f"{what}: non-finite GPU output"
-    assert err <= tol, f"{what}: max |gpu - oracle| = {err:.4g} > {tol:.4g} (rms {rms:.4g})"
+    if not want.size:
+        return 0.0, tol
+    excess = np.abs(got - want) - half_ulp_bf16(want)
+    err = float(excess.max())
+    assert err <= tol, f"{what}: max |gpu - oracle| - half bf16 step = {err:.4g} > {tol:.4g} (rms {rms:.4g})"
     return err, tol
 
 

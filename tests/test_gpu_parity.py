@@ -5,7 +5,8 @@ codes and scales, per-token NVFP4 scales, the weight layouts. The L2-input
 codes equal the oracle's codes of the oracle's h except where the oracle's
 value is within accumulation noise of a rounding midpoint. Within the layer's
 tolerance (max |gpu - oracle| <= rel * rms + 1e-3, rel 2e-2 BF16/MXFP8, 5e-2
-NVFP4; the oracle's value taken before its final bf16 rounding): every output
+NVFP4, for the value before the output's final bf16 rounding, i.e. against the
+oracle's exact value with half a bf16 step of the output on top): every output
 at reduced sizes spanning several tiles with ragged tails, and sampled tokens
 at the full workload sizes. Every expected value comes from the oracle.
 """
@@ -96,10 +97,9 @@ def test_forward_matches_oracle_reduced(name):
     assert run.plan.last_status(run.workspace) == 0
 
 
-def _near_midpoint(v, a, b, rel):
-    """v lies within rel of the midpoint of the two neighbouring grid values a, b."""
-    mid = (a + b) / 2
-    return np.abs(v - mid) <= rel * np.maximum(np.abs(v), 1e-30)
+def _near_midpoint(v, a, b, tau):
+    """v lies within tau of the midpoint of the two neighbouring grid values a, b."""
+    return np.abs(v - (a + b) / 2) <= tau
 
 
 @pytest.mark.parametrize("name", ["mxfp8_small", "nvfp4_decode", "nvfp4_shared_norm", "bf16_toy"])
@@ -117,9 +117,12 @@ def test_l2_input_matches_oracle(name):
     parts = OM.forward(case.layer, case.x, case.ids, case.w, return_parts=True)[1]
     h_or = np.stack([parts["h"][r] for r in rows])                      # rows are the oracle's rows too
     h_gpu = G.region_u8(run, T, "h_debug").view(np.float32).reshape(-1, I)[rows].astype(np.float64)
-    rel_err = np.abs(h_gpu - h_or).max() / np.abs(h_or).max()
-    assert rel_err < 1e-4, rel_err
-    DELTA = 1e-4                                                         # allowed distance to a midpoint
+    hmax = np.abs(h_or).max()
+    rel_err = np.abs(h_gpu - h_or).max() / hmax
+    assert rel_err < 1e-5, rel_err
+    # fp32 accumulation noise of h (the GPU is ~1.5e-7 of max|h| off the fp64 oracle);
+    # a code may differ only where the oracle's value is this close to a rounding midpoint
+    TAU = 1e-6 * hmax
 
     codes, sf = OM.l2_input_codes(h_or.astype(np.float32), shape.fmt, case.layer.a2)
     hq = G.region_u8(run, T, "hq")
@@ -127,7 +130,7 @@ def test_l2_input_matches_oracle(name):
         got = hq.reshape(-1, I * 2)[rows].view(np.uint16)
         diff = got != codes
         a, b = OF.bf16_bits_to_f64(got[diff]), OF.bf16_bits_to_f64(codes[diff])
-        assert np.all(_near_midpoint(h_or[diff], a, b, DELTA))
+        assert np.all(_near_midpoint(h_or[diff], a, b, TAU))
         assert diff.mean() < 1e-3
         return
     fmt = shape.fmt
@@ -141,7 +144,7 @@ def test_l2_input_matches_oracle(name):
     if fmt == "mxfp8":
         e = sf[sf_diff].astype(np.int64) - 127
         bound = np.ldexp(448.0, np.minimum(e, got_sf[sf_diff].astype(np.int64) - 127))
-        assert np.all(np.abs(amax[sf_diff] - bound) <= DELTA * bound)
+        assert np.all(np.abs(amax[sf_diff] - bound) <= TAU)
         deq_or = OF.mxfp8_dequantize(codes, sf)
         deq_gpu = OF.mxfp8_dequantize(got_codes, got_sf)
         scale = OF.UE8M0_TABLE[sf].repeat(g, axis=1)
@@ -150,7 +153,7 @@ def test_l2_input_matches_oracle(name):
         a2 = np.float32(case.layer.a2)
         ratio = amax / (float(a2) * 6.0)
         assert np.all(_near_midpoint(ratio[sf_diff], OF.E4M3_TABLE[sf[sf_diff]], OF.E4M3_TABLE[got_sf[sf_diff]],
-                                     DELTA) | (sf[sf_diff] == got_sf[sf_diff]))
+                                     TAU / (float(a2) * 6.0)))
         deq_or = OF.nvfp4_dequantize(codes, sf, a2)
         deq_gpu = OF.nvfp4_dequantize(got_codes, got_sf, a2)
         eff = (OF.E4M3_TABLE[sf] * float(a2)).repeat(g, axis=1)
@@ -162,7 +165,7 @@ def test_l2_input_matches_oracle(name):
     bad = dv & same_block
     # a differing value in a block with the same scale is the other neighbour of a midpoint
     assert np.all(np.abs(deq_gpu[bad] - deq_or[bad]) <= step[bad] * (1 + 1e-9))
-    assert np.all(_near_midpoint(h_or[bad], deq_gpu[bad], deq_or[bad], DELTA))
+    assert np.all(_near_midpoint(h_or[bad], deq_gpu[bad], deq_or[bad], TAU))
     assert bad.mean() < 1e-3, bad.mean()
 
 
