@@ -229,7 +229,7 @@ def run_reference(args, shape: S.MoeShape):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    n_tok = CPU_SAMPLE_TOKENS[shape.name]
+    n_tok = CPU_SAMPLE_TOKENS[shape.name.split("+")[0]]
     if args.warmup > 0:
         oracle_sample(shape, 0, 1)
     total_s, total_tok, cores = 0.0, 0, 1
@@ -388,7 +388,7 @@ def run_ours(args, shape: S.MoeShape):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        n_tok = CPU_SAMPLE_TOKENS[shape.name]
+        n_tok = CPU_SAMPLE_TOKENS[shape.name.split("+")[0]]
         dt, nt, cores = oracle_sample(shape, 0, n_tok)
         cpu = {"value": round(nt / dt, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"first {nt} tokens of {shape.name} (NumPy fp64 oracle, {dt:.1f} s)"}
@@ -425,8 +425,13 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=S.WORKLOAD_ORDER, default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, help="profiling only: override the workload's T")
+    ap.add_argument("--experts", type=int, help="profiling only: override the workload's E")
     args = ap.parse_args(argv)
     shape = S.WORKLOADS[args.workload]
+    over = {k: v for k, v in (("T", args.tokens), ("E", args.experts)) if v}
+    if over:
+        shape = S.shrink(shape, name=shape.name + "+" + ",".join(f"{k}={v}" for k, v in over.items()), **over)
     if args.impl == "reference":
         return run_reference(args, shape)
     return run_ours(args, shape)
