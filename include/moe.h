@@ -269,6 +269,29 @@ int moe_workspace_region(moe_plan_t plan, int32_t num_tokens, int32_t which,
 int moe_plan_enable_timing(moe_plan_t plan, int32_t enable);
 int moe_plan_kernel_times(moe_plan_t plan, float* ms, int32_t count);
 
+/* ---------------------------------------------------------------- permutation without a workspace */
+
+/*
+ * The routing permutation of moe_forward (per-expert counts, BLOCK_M = 128
+ * padded segment offsets, stable scatter) for callers that must not allocate
+ * device memory: a runtime that owns all of HBM through its own pools, or a
+ * path where a cudaMalloc is not allowed. The paper has no counterpart of this
+ * entry point; it exists for such callers only.
+ *
+ *   topk_ids        device int32 [T, k], -1 masks a slot (ids outside [-1, E)
+ *                   are treated as masked)
+ *   inv_perm        device int32 [T, k] (output): padded row of each slot, -1 if masked
+ *   expert_offsets  device int32 [E + 1] (output): segment starts, [E] = padded total
+ * Scratch lives in a fixed device array inside libmoe.so (about 1.06 MB per
+ * GPU, held until the process exits): T * k + E * 127 must be <= 262144
+ * (else MOE_ERR_CAPACITY, nothing launched); 1 <= k <= 32, 1 <= E <= 512.
+ * The first call on a device sets that device up (looks up the array's
+ * address); make it before any stream capture. Calls share the array: calls
+ * whose GPU work overlaps race. Allocates nothing.
+ */
+int moe_permute_noalloc(const int32_t* topk_ids, int32_t num_tokens, int32_t top_k, int32_t num_experts,
+                        int32_t* inv_perm, int32_t* expert_offsets, void* stream);
+
 /* Static string for a status code. */
 const char* moe_error_string(int32_t status);
 

@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
             "moe_workspace_region": [P, I32, I32, P, P],
             "moe_plan_enable_timing": [P, I32],
             "moe_plan_kernel_times": [P, P, I32],
+            "moe_permute_noalloc": [P, I32, I32, I32, P, P, P],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -107,6 +108,22 @@ def _ptr(t) -> int | None:
 def _stream(stream) -> int:
     s = torch.cuda.current_stream() if stream is None else stream
     return s.cuda_stream
+
+
+def permute_noalloc(topk_ids: torch.Tensor, num_experts: int, inv_perm: torch.Tensor | None = None,
+                    expert_offsets: torch.Tensor | None = None, stream=None):
+    """moe_permute_noalloc: the routing permutation with the library's fixed scratch array
+    (for callers that must not allocate device memory; the output tensors are the
+    caller's). Returns (inv_perm int32 [T, k], expert_offsets int32 [E + 1])."""
+    T, k = topk_ids.shape
+    if inv_perm is None:
+        inv_perm = torch.empty((T, k), dtype=torch.int32, device=topk_ids.device)
+    if expert_offsets is None:
+        expert_offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=topk_ids.device)
+    _check("moe_permute_noalloc", lib().moe_permute_noalloc(
+        _ptr(topk_ids) if T else None, T, k, num_experts, _ptr(inv_perm) if T else None, _ptr(expert_offsets),
+        _stream(stream)))
+    return inv_perm, expert_offsets
 
 
 @dataclass
