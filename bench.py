@@ -39,6 +39,14 @@ PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustaine
 TENSOR_RATIO = {"bf16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0}
 ELEM_BYTES = {"bf16": 2.0, "mxfp8": 1.0, "nvfp4": 0.5}
 SF_PER_ELEM = {"bf16": 0.0, "mxfp8": 1.0 / 32, "nvfp4": 1.0 / 16}
+# DRAM bytes (read + write) per launch from one ncu capture of the current kernels
+# (profiles/grouped_gemm_*.md); an entry must be removed when its kernel changes
+NCU_TRAFFIC = {
+    ("mxfp8_small", "l1"): (225.152768e6 + 4.943360e6, "profiles/grouped_gemm_mxfp8_small.md"),
+    ("mxfp8_small", "l2"): (110.385408e6 + 3.610624e6, "profiles/grouped_gemm_mxfp8_small.md"),
+    ("nvfp4_decode", "l1"): (4.247895e9 + 4.720384e6, "profiles/grouped_gemm_nvfp4_decode.md"),
+    ("nvfp4_decode", "l2"): (2.093047e9 + 17.182464e6, "profiles/grouped_gemm_nvfp4_decode.md"),
+}
 # tokens the CPU oracle processes per timed sample (about 10-30 s of host work)
 CPU_SAMPLE_TOKENS = {"bf16_toy": 64, "mxfp8_small": 24, "nvfp4_decode": 3, "mxfp8_prefill_zipf": 12,
                      "nvfp4_shared_norm": 6}
@@ -383,6 +391,8 @@ def run_ours(args, shape: S.MoeShape):
     dominant = max(avg_k, key=avg_k.get)
     peaks, source = load_peaks()
     rl = roofline(dominant, work, avg_k[dominant], peaks, source, sustained=False)
+    if (shape.name, dominant) in NCU_TRAFFIC:
+        rl["traffic"], rl["traffic_source"] = NCU_TRAFFIC[(shape.name, dominant)]
     rl["kernel_ms"] = {k_: round(v, 4) for k_, v in avg_k.items()}
     sec = sum(step_ms) / 1e3 / args.steps
 
