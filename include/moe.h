@@ -56,6 +56,8 @@ extern "C" {
 #define MOE_ACT_SWIGLU 0
 
 #define MOE_FLAG_DEBUG_H  1u       /* also keep the fp32 L1 epilogue output h in the workspace */
+#define MOE_FLAG_TILE_128 2u       /* 128-wide GEMM tiles with double-buffered accumulators */
+#define MOE_FLAG_TILE_256 4u       /* 256-wide GEMM tiles (the default) */
 
 /* ---------------------------------------------------------------- config / plan */
 
@@ -138,19 +140,20 @@ int moe_config_workspace_size(const moe_config_t* cfg, int32_t num_tokens, size_
  * vpe (values per byte-element): 1 for BF16 (2-byte elements) and MXFP8, 2 for NVFP4.
  *
  * Kernel layout (dst of moe_transform_weights, what moe_forward reads):
- *   w13  [E, 2I, H/vpe] with rows interleaved per 256-row tile: kernel row
- *        256*b + 128*half + r holds checkpoint row half*I + 128*b + r
- *        (half 0 = gate, 1 = up; 0 <= r < 128), so one 256-wide N tile holds
- *        128 gate and the matching 128 up columns (the pages interleave by 8,
+ *   w13  [E, 2I, H/vpe] with rows interleaved per 128-row block: kernel row
+ *        128*b + 64*half + r holds checkpoint row half*I + 64*b + r
+ *        (half 0 = gate, 1 = up; 0 <= r < 64), so every 128-row block holds 64
+ *        gate and the matching 64 up rows (the pages interleave by 8,
  *        DeepGemmMegaMoEExperts._kernel_layout_shard).
  *   w2   unchanged.
- *   *_sf scale-factor atoms for the tensor-memory copy: for each expert,
- *        256-row N tile nt, K stage ks (128 bytes of codes along K), atom s,
- *        128-row half nb: one 512-byte atom holding 128 rows x 4 scales, byte
+ *   *_sf scale-factor atoms for the tensor-memory copy: for each expert, K
+ *        stage ks (128 bytes of codes along K), 128-row block nb and atom s:
+ *        one 512-byte atom holding 128 rows x 4 scales, byte
  *        (n % 32) * 16 + ((n % 128) / 32) * 4 + (scale index % 4), i.e. row
  *        128c + 32j + i sits in 32-bit word 4i + j (the pages' UTCCP row
- *        permutation, _kernel_layout_shard), laid out [E][N/256][K stages][S][2][512]
- *        with S = 1 (MXFP8) or 4 (NVFP4) atoms per stage. Rows past N are zero.
+ *        permutation, _kernel_layout_shard), laid out [E][K stages][NB][S][512]
+ *        with NB = round_up(N, 256) / 128 and S = 1 (MXFP8) or 4 (NVFP4)
+ *        atoms per stage. Rows past N are zero.
  *   *_gs copied unchanged.
  * Sizes of each kernel-layout tensor: moe_weight_layout_size.
  */

@@ -141,11 +141,11 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [E][N][row_bytes] weights, loaded as 128-byte x BN-row tiles of one expert
-bool map_3d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t N, uint64_t E) {
+// [E][N][row_bytes] weights, loaded as 128-byte x bn-row tiles of one expert
+bool map_3d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t N, uint64_t E, uint32_t bn) {
     cuuint64_t dims[3] = {row_bytes, N, E};
     cuuint64_t strides[2] = {row_bytes, row_bytes * N};
-    cuuint32_t box[3] = {(cuuint32_t)BK_BYTES, (cuuint32_t)BN, 1};
+    cuuint32_t box[3] = {(cuuint32_t)BK_BYTES, bn, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -205,10 +205,7 @@ int moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     if (!get_encode()) return MOE_ERR_CUDA;
     CUDA_TRY(route_prepare(MAX_EXPERTS));
-    for (int f = MOE_FMT_BF16; f <= MOE_FMT_NVFP4; ++f) {
-        CUDA_TRY(gemm_prepare(f, true));
-        CUDA_TRY(gemm_prepare(f, false));
-    }
+    for (int f = MOE_FMT_BF16; f <= MOE_FMT_NVFP4; ++f) CUDA_TRY(gemm_prepare(f));
     moe_plan_s* p = new (std::nothrow) moe_plan_s;
     if (!p) return MOE_ERR_INVALID_ARG;
     p->cfg = *cfg;
@@ -291,9 +288,9 @@ static int64_t weight_bytes(const moe_config_t& c, int which) {
         case MOE_W2:
         case MOE_SHARED_W2: return E * H * fmt_row_bytes(fmt, I);
         case MOE_W13_SF:
-        case MOE_SHARED_W13_SF: return E * ceil_div(2 * I, BN) * fmt_k_stages(fmt, H) * S * 2 * ATOM_BYTES;
+        case MOE_SHARED_W13_SF: return E * fmt_k_stages(fmt, H) * wt_sf_blocks(2 * I) * S * ATOM_BYTES;
         case MOE_W2_SF:
-        case MOE_SHARED_W2_SF: return E * ceil_div(H, BN) * fmt_k_stages(fmt, I) * S * 2 * ATOM_BYTES;
+        case MOE_SHARED_W2_SF: return E * fmt_k_stages(fmt, I) * wt_sf_blocks(H) * S * ATOM_BYTES;
         case MOE_W13_GS:
         case MOE_W2_GS: return d.fmt == MOE_FMT_NVFP4 ? 4 * E : 0;
         default: return -1;
@@ -346,7 +343,18 @@ int moe_transform_shared_weights(moe_plan_t plan, const moe_weights_t* src, moe_
 }
 
 // one expert MLP pass (L1 then L2) over row tiles of the given A buffers
-static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, const void* xq, const uint8_t* xsf, int64_t rows,
+// N-tile width. Measured on GB300 at every workload, 256-wide tiles (one accumulator,
+// 4-stage ring) beat 128-wide tiles with double-buffered accumulators (6 stages): the
+// narrower tile reloads the A tile twice as often per weight byte. So 256 unless
+// MOE_FLAG_TILE_128 forces 128.
+static int choose_bn(const moe_config_t& c, int64_t rows_per_expert) {
+    (void)rows_per_expert;
+    if (c.flags & MOE_FLAG_TILE_128) return 128;
+    return 256;
+}
+
+static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, int64_t rows_per_expert, const void* xq,
+                   const uint8_t* xsf, int64_t rows,
                    const moe_weights_t* w, const int* m_tiles_dev, int m_tiles_host, int64_t m_tiles_max,
                    const int* tile_expert, const int* src, int m_valid, const float* x_scale, const float* a2,
                    uint8_t* hq, uint8_t* hsf, float* h_debug, __nv_bfloat16* y, int* err, bool activation,
@@ -366,13 +374,15 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, const 
     g.act_beta = activation ? c.act_beta : 0.0f;
     g.act_clamp = c.act_clamp;
     g.act_has_clamp = activation ? c.act_has_clamp : 0;
+    const int bn = choose_bn(c, rows_per_expert);
     // L1: [rows, H] x w13[e]^T -> h [rows, I]
     if (!map_2d(&ta, xq, fmt_row_bytes(fmt, H), rows, BM)) return MOE_ERR_CUDA;
-    if (!map_3d(&tb, w->w13, fmt_row_bytes(fmt, H), 2 * (uint64_t)I, E)) return MOE_ERR_CUDA;
+    if (!map_3d(&tb, w->w13, fmt_row_bytes(fmt, H), 2 * (uint64_t)I, E, bn)) return MOE_ERR_CUDA;
     g.sfa = xsf;
     g.sfb = (const uint8_t*)w->w13_sf;
     g.nks = (int)fmt_k_stages(fmt, H);
-    g.n_tiles = (int)ceil_div(2 * I, BN);
+    g.n_tiles = (int)ceil_div(2 * I, bn);
+    g.sf_blocks = (int)wt_sf_blocks(2 * I);
     g.N = 2 * I;
     g.x_scale = x_scale;
     g.gscale = w->w13_gs;
@@ -385,15 +395,16 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, const 
     const int grid1 = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, m_tiles_max * g.n_tiles));
     {
         KernelTimer kt(p, kid1, st);
-        CUDA_TRY(launch_gemm(fmt, true, ta, tb, g, grid1, st));
+        CUDA_TRY(launch_gemm(fmt, true, bn, ta, tb, g, grid1, st));
     }
     // L2: h [rows, I] x w2[e]^T -> y [rows, H]
     if (!map_2d(&ta, hq, fmt_row_bytes(fmt, I), rows, BM)) return MOE_ERR_CUDA;
-    if (!map_3d(&tb, w->w2, fmt_row_bytes(fmt, I), H, E)) return MOE_ERR_CUDA;
+    if (!map_3d(&tb, w->w2, fmt_row_bytes(fmt, I), H, E, bn)) return MOE_ERR_CUDA;
     g.sfa = hsf;
     g.sfb = (const uint8_t*)w->w2_sf;
     g.nks = (int)fmt_k_stages(fmt, I);
-    g.n_tiles = (int)ceil_div(H, BN);
+    g.n_tiles = (int)ceil_div(H, bn);
+    g.sf_blocks = (int)wt_sf_blocks(H);
     g.N = H;
     g.gscale = w->w2_gs;
     g.y = y;
@@ -401,7 +412,7 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, const 
     const int grid2 = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, m_tiles_max * g.n_tiles));
     {
         KernelTimer kt(p, kid1 + 1, st);
-        CUDA_TRY(launch_gemm(fmt, false, ta, tb, g, grid2, st));
+        CUDA_TRY(launch_gemm(fmt, false, bn, ta, tb, g, grid2, st));
     }
     return MOE_OK;
 }
@@ -458,14 +469,14 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
         CUDA_TRY(launch_dispatch(da, st));
     }
 
-    int rc = run_mlp(plan, MOE_KERNEL_L1, d.fmt, d.E, d.I, d.H, R(R_XQ), R(R_XSF), L.m_pad_max, weights, meta + 1, 0, L.m_tiles_max,
+    int rc = run_mlp(plan, MOE_KERNEL_L1, d.fmt, d.E, d.I, d.H, ceil_div((int64_t)T * d.k, d.E), R(R_XQ), R(R_XSF), L.m_pad_max, weights, meta + 1, 0, L.m_tiles_max,
                      (const int*)R(R_TILE_EXPERT), (const int*)R(R_SRC), 0, (const float*)R(R_XSCALE), l2_act_scale,
                      R(R_HQ), R(R_HSF), (c.flags & MOE_FLAG_DEBUG_H) ? (float*)R(R_HDBG) : nullptr,
                      (__nv_bfloat16*)R(R_Y), err, true, st);
     if (rc != MOE_OK) return rc;
     if (d.Is > 0) {
         const int tiles = (int)(L.t_pad / BM);
-        rc = run_mlp(plan, MOE_KERNEL_SHARED_L1, d.sfmt, 1, d.Is, d.H, R(R_SXQ), R(R_SXSF), L.t_pad, shared, nullptr, tiles, tiles, nullptr,
+        rc = run_mlp(plan, MOE_KERNEL_SHARED_L1, d.sfmt, 1, d.Is, d.H, T, R(R_SXQ), R(R_SXSF), L.t_pad, shared, nullptr, tiles, tiles, nullptr,
                      nullptr, T, nullptr, nullptr, R(R_SHQ), R(R_SHSF), nullptr, (__nv_bfloat16*)R(R_SY), err, false,
                      st);
         if (rc != MOE_OK) return rc;

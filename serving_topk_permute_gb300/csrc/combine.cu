@@ -38,20 +38,18 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineA
     __syncthreads();
 
     float acc[COMBINE_MAX_CHUNKS][8];
+    // chunk-outer, slot-inner: the k row loads of one chunk are independent and can all be
+    // in flight; each element is still summed in ascending j
 #pragma unroll
-    for (int i = 0; i < COMBINE_MAX_CHUNKS; ++i)
+    for (int i = 0; i < COMBINE_MAX_CHUNKS; ++i) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-
-    for (int j = 0; j < a.k; ++j) {
-        const int r = s_rows[j];
-        if (r < 0) continue;
-        const float w = s_w[j];
-        const uint4* yrow = reinterpret_cast<const uint4*>(a.y + (int64_t)r * a.H);
-#pragma unroll
-        for (int i = 0; i < COMBINE_MAX_CHUNKS; ++i) {
-            const int c = tid + i * COMBINE_THREADS;
-            if (c < nchunks) acc_bf16x8(acc[i], yrow[c], w);
+        const int c = tid + i * COMBINE_THREADS;
+        if (c >= nchunks) continue;
+#pragma unroll 4
+        for (int j = 0; j < a.k; ++j) {
+            const int r = s_rows[j];
+            if (r >= 0) acc_bf16x8(acc[i], reinterpret_cast<const uint4*>(a.y + (int64_t)r * a.H)[c], s_w[j]);
         }
     }
     if (a.ys) {

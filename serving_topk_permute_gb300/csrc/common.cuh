@@ -15,13 +15,13 @@ namespace moe {
 
 // ------------------------------------------------------------------ tile geometry
 constexpr int BM = 128;            // rows per MMA tile (= BLOCK_M of the routing)
-constexpr int BN = 256;            // columns per MMA tile (weight rows)
+constexpr int BN_MAX = 256;        // widest MMA tile (weight rows); tiles are 128 or 256 wide
+constexpr int NBLK = 128;          // weight rows per scale-atom block and per gate/up interleave unit
 constexpr int BK_BYTES = 128;      // bytes of codes per K stage (one 128-byte swizzle row)
 constexpr int ATOM_BYTES = 512;    // one scale-factor atom: 128 rows x 4 scales
-constexpr int NUM_STAGES = 4;
-constexpr int GEMM_THREADS = 192;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 epilogue
+constexpr int EPI_WARPS = 16;      // 4 per tensor-memory lane quarter, each on a quarter of the columns
+constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA producer, warp 1 MMA issuer, then epilogue
 constexpr int TMEM_COLS = 512;
-constexpr int ACC_COLS = BN;       // fp32 accumulator columns
 
 // per-format constants
 __host__ __device__ constexpr int fmt_elem_bits(int fmt) { return fmt == MOE_FMT_BF16 ? 16 : (fmt == MOE_FMT_MXFP8 ? 8 : 4); }
@@ -43,13 +43,24 @@ __host__ __device__ inline int64_t act_sf_offset(int64_t r, int64_t kb, int S, i
     return ((mt * nks + ks) * S + s) * ATOM_BYTES + (m % 32) * 16 + (m / 32) * 4 + b;
 }
 
-// Byte offset of scale block kb of kernel-layout weight row n of expert e in a
-// weight scale-atom array laid out [E][N tiles][K stage][S atoms][2 halves][512].
+// Weight scale atoms are laid out [E][K stage][N blocks][S atoms][512] with 128-row
+// blocks and N blocks = round_up(N, 256) / 128 (rows past N are zero), so the atoms of
+// one K stage of any 128- or 256-row tile are one contiguous run.
+__host__ __device__ inline int64_t wt_sf_blocks(int64_t N) { return (N + BN_MAX - 1) / BN_MAX * (BN_MAX / NBLK); }
+
+// Byte offset of scale block kb of kernel-layout weight row n of expert e.
 __host__ __device__ inline int64_t wt_sf_offset(int64_t e, int64_t n, int64_t kb, int S, int64_t nks,
-                                                int64_t n_tiles) {
-    const int64_t nt = n / BN, nb = (n % BN) / BM, m = n % BM;
+                                                int64_t n_blocks) {
+    const int64_t nb = n / NBLK, m = n % NBLK;
     const int64_t ks = kb / (4 * S), s = (kb / 4) % S, b = kb % 4;
-    return ((((e * n_tiles + nt) * nks + ks) * S + s) * 2 + nb) * ATOM_BYTES + (m % 32) * 16 + (m / 32) * 4 + b;
+    return ((((e * nks + ks) * n_blocks + nb) * S + s)) * ATOM_BYTES + (m % 32) * 16 + (m / 32) * 4 + b;
+}
+
+// w13 gate/up interleave: kernel row 128 b + 64 h + r (h 0 = gate, 1 = up, r < 64)
+// holds checkpoint row h * I + 64 b + r.
+__host__ __device__ inline int64_t w13_src_row(int64_t n, int64_t I) {
+    const int64_t b = n / NBLK, h = (n % NBLK) / 64, r = n % 64;
+    return h * I + b * 64 + r;
 }
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -218,18 +229,18 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
-// Instruction descriptors (M = 128, N = BN, both operands K-major).
+// Instruction descriptors (M = 128, N = n, both operands K-major).
 // kind::f16: D fp32 (bits 4-5 = 1), A/B bf16 (bits 7-9, 10-12 = 1), N>>3 at 17, M>>4 at 24.
-__host__ __device__ constexpr uint32_t idesc_bf16() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 // kind::mxf8f6f4: A/B E4M3 (0), scale type UE8M0 (bit 23), scale ids: B at 4-5, A at 29-30.
-__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t sf_id) {
-    return (sf_id << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
+__host__ __device__ constexpr uint32_t idesc_mxf8(int n, uint32_t sf_id) {
+    return (sf_id << 4) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
 }
 // kind::mxf4nvf4: A/B E2M1 (1), scale type UE4M3 (bit 23 = 0).
-__host__ __device__ constexpr uint32_t idesc_nvf4() {
-    return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_nvf4(int n) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
 // load 32 consecutive fp32 columns of this warp's 32 lanes (one row per thread)

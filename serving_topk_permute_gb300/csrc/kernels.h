@@ -35,9 +35,10 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st);
 // ------------------------------------------------------------------ grouped GEMM
 struct GemmArgs {
     const uint8_t* sfa;        // activation scale atoms [row tiles][nks][S][512]
-    const uint8_t* sfb;        // weight scale atoms [E][n_tiles][nks][S][2][512]
+    const uint8_t* sfb;        // weight scale atoms [E][nks][sf_blocks][S][512]
     int nks;                   // 128-byte K stages
-    int n_tiles;               // 256-column tiles
+    int n_tiles;               // BN-column tiles
+    int sf_blocks;             // 128-row blocks of the weight scale layout (wt_sf_blocks(N))
     int N;                     // output columns (kernel-layout weight rows)
     const int* m_tiles_dev;    // number of 128-row tiles on the device (or null)
     int m_tiles_host;          // used when m_tiles_dev is null
@@ -62,9 +63,9 @@ struct GemmArgs {
     int* err;
     unsigned long long timeout_ns;
 };
-size_t gemm_smem_bytes(int fmt);
-cudaError_t gemm_prepare(int fmt, bool l1);   // sets the dynamic shared memory attribute
-cudaError_t launch_gemm(int fmt, bool l1, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t gemm_prepare(int fmt);   // sets the dynamic shared memory attribute of every variant
+// bn: 128 or 256 (the tile width; the B tensor map's box must be bn rows)
+cudaError_t launch_gemm(int fmt, bool l1, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                         int grid, cudaStream_t st);
 
 // ------------------------------------------------------------------ combine

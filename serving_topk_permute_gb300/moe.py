@@ -24,6 +24,7 @@ W13, W13_SF, W2, W2_SF, SHARED_W13, SHARED_W13_SF, SHARED_W2, SHARED_W2_SF, W13_
 REGIONS = {"counts": 0, "offsets": 1, "src": 2, "inv_perm": 3, "xq": 4, "xsf": 5, "x_scale": 6, "hq": 7,
            "hsf": 8, "h_debug": 9, "y": 10, "meta": 11, "shared_y": 12}
 FLAG_DEBUG_H = 1
+FLAG_TILE = {0: 0, 128: 2, 256: 4}   # GEMM tile width: 0 = chosen by rows per expert
 KERNELS = ["route", "dispatch", "l1", "l2", "shared_l1", "shared_l2", "combine"]
 
 
@@ -142,12 +143,14 @@ class LayerConfig:
     post_norm: bool = False
     norm_eps: float = 1e-6
     debug_h: bool = False
+    tile: int = 0
 
     def to_c(self) -> Config:
         return Config(self.num_experts, self.hidden, self.inter, self.top_k, self.max_tokens, FORMATS[self.fmt], 0,
                       self.act_alpha, self.act_beta, 0.0 if self.act_clamp is None else self.act_clamp,
                       0 if self.act_clamp is None else 1, self.shared_inter, FORMATS[self.shared_fmt],
-                      1 if self.post_norm else 0, self.norm_eps, FLAG_DEBUG_H if self.debug_h else 0)
+                      1 if self.post_norm else 0, self.norm_eps,
+                      (FLAG_DEBUG_H if self.debug_h else 0) | FLAG_TILE[self.tile])
 
 
 def validate(cfg: LayerConfig) -> int:

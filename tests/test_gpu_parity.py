@@ -88,11 +88,13 @@ def test_routing_and_dispatch_bit_exact_full_size(name):
 
 # ----------------------------------------------------------------------------- outputs, reduced sizes, every element
 
+@pytest.mark.parametrize("tile", [128, 256])
 @pytest.mark.parametrize("name", list(REDUCED))
-def test_forward_matches_oracle_reduced(name):
+def test_forward_matches_oracle_reduced(name, tile):
+    """Both GEMM tile widths (128: double-buffered accumulators; 256: one accumulator)."""
     shape = REDUCED[name]
     case = G.float_case(shape)
-    run = G.run_gpu(case)
+    run = G.run_gpu(case, tile=tile)
     G.assert_close(G.out_f64(run), G.oracle_out(case), shape.fmt, name)
     assert run.plan.last_status(run.workspace) == 0
 
@@ -282,35 +284,33 @@ def test_activation_variants(alpha, beta, clamp):
 # ----------------------------------------------------------------------------- weight layout
 
 def _expected_interleave(w13: np.ndarray, I: int) -> np.ndarray:
-    """Kernel row 256b + 128h + r holds checkpoint row h*I + 128b + r."""
-    E = w13.shape[0]
+    """Kernel row 128b + 64h + r holds checkpoint row h*I + 64b + r (h 0 gate, 1 up, r < 64)."""
     out = np.empty_like(w13)
     for n in range(2 * I):
-        b, h, r = n // 256, (n % 256) // 128, n % 128
-        out[:, n] = w13[:, h * I + 128 * b + r]
+        b, h, r = n // 128, (n % 128) // 64, n % 64
+        out[:, n] = w13[:, h * I + 64 * b + r]
     return out
 
 
 def _expected_sf_atoms(sf: np.ndarray, N: int, K: int, g: int, interleave: bool, I: int) -> np.ndarray:
     """Row 32j+i / scale b of 4 at byte 16i + 4j + b of a 512-byte atom (the UTCCP row
-    permutation 128c + 32j + i -> 128c + 4i + j in 32-bit words), atoms [E][N/256][stage][S][2]."""
+    permutation 128c + 32j + i -> 128c + 4i + j in 32-bit words), atoms
+    [E][K stage][128-row block][S], blocks = round_up(N, 256) / 128."""
     E = sf.shape[0]
     S_atoms = 1 if g == 32 else 4
     nkb = K // g
     nks = nkb // (4 * S_atoms)
-    nt_n = -(-N // 256)
-    out = np.zeros((E, nt_n, nks, S_atoms, 2, 512), np.uint8)
-    for n in range(nt_n * 256):
-        if n >= N:
-            continue
+    nblk = -(-N // 256) * 2
+    out = np.zeros((E, nks, nblk, S_atoms, 512), np.uint8)
+    for n in range(N):
         row = n
         if interleave:
-            b, h, r = n // 256, (n % 256) // 128, n % 128
-            row = h * I + 128 * b + r
-        nt, nb, m = n // 256, (n % 256) // 128, n % 128
+            b, h, r = n // 128, (n % 128) // 64, n % 64
+            row = h * I + 64 * b + r
+        nb, m = n // 128, n % 128
         for kb in range(nkb):
             ks, s, bb = kb // (4 * S_atoms), (kb // 4) % S_atoms, kb % 4
-            out[:, nt, ks, s, nb, (m % 32) * 16 + (m // 32) * 4 + bb] = sf[:, row, kb]
+            out[:, ks, nb, s, (m % 32) * 16 + (m // 32) * 4 + bb] = sf[:, row, kb]
     return out.reshape(-1)
 
 
