@@ -206,6 +206,7 @@ int moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     if (!get_encode()) return MOE_ERR_CUDA;
     CUDA_TRY(route_prepare(MAX_EXPERTS));
     for (int f = MOE_FMT_BF16; f <= MOE_FMT_NVFP4; ++f) CUDA_TRY(gemm_prepare(f));
+    CUDA_TRY(combine_prepare());
     moe_plan_s* p = new (std::nothrow) moe_plan_s;
     if (!p) return MOE_ERR_INVALID_ARG;
     p->cfg = *cfg;
@@ -448,7 +449,7 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
 
     {
         KernelTimer kt(plan, MOE_KERNEL_ROUTE, st);
-        CUDA_TRY(launch_route(topk_ids, T, d.k, d.E, (int*)R(R_CNT), (int*)R(R_OFF), (int*)R(R_SRC), (int*)R(R_INV),
+        CUDA_TRY(launch_route(topk_ids, T, d.k, d.E, BM, (int*)R(R_CNT), (int*)R(R_OFF), (int*)R(R_SRC), (int*)R(R_INV),
                           (int*)R(R_TILE_EXPERT), meta, err, st));
     }
     DispatchArgs da{};

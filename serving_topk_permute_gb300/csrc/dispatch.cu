@@ -4,8 +4,8 @@
 // per token; vllm.model_executor.layers.fused_moe, DeepGemmExperts.apply:
 // deepgemm_moe_permute writes a1q_perm).
 //
-// One CTA of 128 threads per token. Each thread owns 8-element chunks
-// c = tid + 128 i of the row, loaded as one 128-bit bf16x8 vector each, kept in
+// One CTA of 256 threads per token. Each thread owns 8-element chunks
+// c = tid + 256 i of the row, loaded as one 128-bit bf16x8 vector each, kept in
 // registers. Per format:
 //   BF16   the 16-byte chunk is copied as is
 //   MXFP8  a 32-element block is 4 neighbouring threads: block amax by two xor
@@ -24,8 +24,8 @@
 
 namespace moe {
 
-constexpr int DISPATCH_THREADS = 128;
-constexpr int DISPATCH_MAX_CHUNKS = 16;  // H <= 16 * 128 * 8 = 16384
+constexpr int DISPATCH_THREADS = 256;
+constexpr int DISPATCH_MAX_CHUNKS = 8;   // H <= 8 * 256 * 8 = 16384
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};

@@ -9,12 +9,12 @@
 namespace moe {
 
 // ------------------------------------------------------------------ routing
-// Histogram, BLOCK_M-padded offsets, stable scatter (one CTA). Writes cnt[E],
-// off[E+1], src[M_pad] (-1 padding), inv[T*k] (-1 masked), tile_expert[M_pad/BM],
-// meta[0] = M_pad, meta[1] = M_pad / BM.
+// Histogram, BLOCK_M (bm)-padded offsets, stable scatter (one CTA). Writes cnt[E],
+// off[E+1], src[M_pad] (-1 padding), inv[T*k] (-1 masked), tile_expert[M_pad/bm],
+// meta[0] = M_pad, meta[1] = M_pad / bm.
 size_t route_smem_bytes(int E);
 cudaError_t route_prepare(int E);   // sets the dynamic shared memory attribute (E <= 512)
-cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int* cnt, int* off, int* src, int* inv,
+cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int bm, int* cnt, int* off, int* src, int* inv,
                          int* tile_expert, int* meta, int* err, cudaStream_t st);
 
 // ------------------------------------------------------------------ dispatch quantisation
@@ -79,6 +79,7 @@ struct CombineArgs {
     float eps;
     __nv_bfloat16* out;        // [T, H]
 };
+cudaError_t combine_prepare();   // allows the norm's [H] fp32 shared-memory row (H <= 16384)
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 
 // ------------------------------------------------------------------ weight transform

@@ -78,7 +78,7 @@ extern "C" int moe_permute_noalloc(const int32_t* topk_ids, int32_t num_tokens, 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the error word must start at zero; everything else the kernel reads it writes first
     if (cudaMemsetAsync(s + OFF_ERR, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
-    if (moe::launch_route(topk_ids, num_tokens, top_k, num_experts, s + OFF_CNT, expert_offsets, s + OFF_SRC,
+    if (moe::launch_route(topk_ids, num_tokens, top_k, num_experts, moe::BM, s + OFF_CNT, expert_offsets, s + OFF_SRC,
                           inv_perm, s + OFF_TILES, s + OFF_META, s + OFF_ERR, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;

@@ -3,6 +3,7 @@
 // DeepGemmExperts.workspace_shapes: compute_aligned_M, M_sum % block_m == 0;
 // DeepGemmExperts.apply: deepgemm_moe_permute -> expert ids and inv_perm).
 //
+// Segments are padded to BLOCK_M = bm rows (128, or 256 for the CTA-pair GEMM).
 // One CTA of 1024 threads (32 warps). Warp w owns a contiguous chunk of the
 // flat slots s = t*k + j.
 //   pass 1  each warp counts its chunk per expert into its own shared row
@@ -22,11 +23,12 @@ namespace moe {
 
 constexpr int ROUTE_THREADS = 1024;
 constexpr int ROUTE_WARPS = ROUTE_THREADS / 32;
+constexpr int RB = 8;  // 32-slot groups whose ids are loaded together
 
 __global__ void __launch_bounds__(ROUTE_THREADS, 1)
-    route_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int* __restrict__ cnt, int* __restrict__ off,
-                 int* __restrict__ src, int* __restrict__ inv, int* __restrict__ tile_expert, int* __restrict__ meta,
-                 int* err) {
+    route_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int bm, int* __restrict__ cnt,
+                 int* __restrict__ off, int* __restrict__ src, int* __restrict__ inv, int* __restrict__ tile_expert,
+                 int* __restrict__ meta, int* err) {
     extern __shared__ int sm[];
     int* wcnt = sm;                          // [32][E]: per-warp counts, then per-warp running bases
     int* s_off = sm + ROUTE_WARPS * E;       // [E+1]
@@ -40,13 +42,23 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     for (int i = tid; i < ROUTE_WARPS * E; i += ROUTE_THREADS) wcnt[i] = 0;
     __syncthreads();
 
-    // pass 1: per-warp histograms
-    for (int s = beg + lane; s < end; s += 32) {
-        const int e = ids[s];
-        if (e >= 0 && e < E)
-            atomicAdd(&wcnt[warp * E + e], 1);
-        else if (e != -1)
-            set_error(err, MOE_ERR_BAD_EXPERT_ID);
+    // pass 1: per-warp histograms (ids loaded RB groups of 32 at a time: independent loads in flight)
+    for (int s0 = beg; s0 < end; s0 += 32 * RB) {
+        int ev[RB];
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+            const int s = s0 + 32 * u + lane;
+            ev[u] = s < end ? ids[s] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+            if (s0 + 32 * u >= end) break;  // warp-uniform
+            const int e = ev[u];
+            if (e >= 0 && e < E)
+                atomicAdd(&wcnt[warp * E + e], 1);
+            else if (e != -1)
+                set_error(err, MOE_ERR_BAD_EXPERT_ID);
+        }
     }
     __syncthreads();
 
@@ -65,7 +77,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
 
     // block-wide exclusive scan of the padded sizes (E <= 1024: one value per thread)
     {
-        const int v = tid < E ? (int)align_up(s_cnt[tid], BM) : 0;
+        const int v = tid < E ? (int)align_up(s_cnt[tid], bm) : 0;
         int x = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -90,35 +102,46 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     }
     __syncthreads();
     for (int e = tid; e <= E; e += ROUTE_THREADS) off[e] = s_off[e];
+    // every row starts as padding (-1); the scatter below overwrites the routed ones
+    for (int r = tid; r < s_off[E]; r += ROUTE_THREADS) src[r] = -1;
+    __syncthreads();
 
-    // pass 2: stable scatter
+    // pass 2: stable scatter, in ascending slot order (ids again loaded RB groups at a time)
     const unsigned lt = (1u << lane) - 1u;
-    for (int s0 = beg; s0 < end; s0 += 32) {
-        const int s = s0 + lane;
-        const int e = s < end ? ids[s] : -1;
-        const bool routed = s < end && e >= 0 && e < E;
-        const int key = routed ? e : E + lane;  // unrouted lanes never group
-        const unsigned peers = __match_any_sync(0xffffffffu, key);
-        if (routed) {
-            const int row = s_off[e] + wcnt[warp * E + e] + __popc(peers & lt);
-            src[row] = s;
-            inv[s] = row;
-        } else if (s < end) {
-            inv[s] = -1;
+    for (int s0 = beg; s0 < end; s0 += 32 * RB) {
+        int ev[RB];
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+            const int s = s0 + 32 * u + lane;
+            ev[u] = s < end ? ids[s] : -1;
         }
-        __syncwarp();
-        if (routed && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
-        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+            if (s0 + 32 * u >= end) break;  // warp-uniform
+            const int s = s0 + 32 * u + lane;
+            const int e = ev[u];
+            const bool routed = s < end && e >= 0 && e < E;
+            const int key = routed ? e : E + lane;  // unrouted lanes never group
+            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            if (routed) {
+                const int row = s_off[e] + wcnt[warp * E + e] + __popc(peers & lt);
+                src[row] = s;
+                inv[s] = row;
+            } else if (s < end) {
+                inv[s] = -1;
+            }
+            __syncwarp();
+            if (routed && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+            __syncwarp();
+        }
     }
 
-    // padding rows and the row-tile -> expert map
-    for (int e = tid; e < E; e += ROUTE_THREADS) {
-        for (int r = s_off[e] + s_cnt[e]; r < s_off[e + 1]; ++r) src[r] = -1;
-        for (int mt = s_off[e] / BM; mt < s_off[e + 1] / BM; ++mt) tile_expert[mt] = e;
-    }
+    // the row-tile -> expert map
+    for (int e = tid; e < E; e += ROUTE_THREADS)
+        for (int mt = s_off[e] / bm; mt < s_off[e + 1] / bm; ++mt) tile_expert[mt] = e;
     if (tid == 0) {
         meta[0] = s_off[E];
-        meta[1] = s_off[E] / BM;
+        meta[1] = s_off[E] / bm;
     }
 }
 
@@ -128,10 +151,10 @@ cudaError_t route_prepare(int E) {
     return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)route_smem_bytes(E));
 }
 
-cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int* cnt, int* off, int* src, int* inv,
+cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int bm, int* cnt, int* off, int* src, int* inv,
                          int* tile_expert, int* meta, int* err, cudaStream_t st) {
     const size_t smem = route_smem_bytes(E);
-    route_kernel<<<1, ROUTE_THREADS, smem, st>>>(ids, T, k, E, cnt, off, src, inv, tile_expert, meta, err);
+    route_kernel<<<1, ROUTE_THREADS, smem, st>>>(ids, T, k, E, bm, cnt, off, src, inv, tile_expert, meta, err);
     return cudaGetLastError();
 }
 
