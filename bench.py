@@ -288,7 +288,7 @@ def run_ours(args, shape: S.MoeShape):
     T = shape.T
     plan = pkg.Plan(pkg.LayerConfig(shape.E, shape.H, shape.I, shape.k, T, shape.fmt, shared_inter=shape.shared_I,
                                     shared_fmt=shape.shared_fmt, post_norm=shape.post_norm,
-                                    norm_eps=shape.norm_eps, tile=args.tile))
+                                    norm_eps=shape.norm_eps, tile=args.tile, cta=args.cta))
     ck = S.torch_code_checkpoint(shape, seed, dev)
     kw = plan.transform_weights({k: v for k, v in ck.items() if k != "w2_input_scale"})
     ks = plan.transform_shared_weights(S.torch_code_checkpoint(shape, seed, dev, shared=True)) \
@@ -437,6 +437,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tile", type=int, choices=[0, 128, 256], default=0,
                     help="GEMM tile width (0: the library's choice by rows per expert)")
+    ap.add_argument("--cta", choices=["auto", "pair", "single"], default="auto",
+                    help="GEMMs on CTA pairs: the library's choice, always or never")
     ap.add_argument("--tokens", type=int, help="profiling only: override the workload's T")
     ap.add_argument("--experts", type=int, help="profiling only: override the workload's E")
     args = ap.parse_args(argv)

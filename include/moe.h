@@ -58,6 +58,8 @@ extern "C" {
 #define MOE_FLAG_DEBUG_H  1u       /* also keep the fp32 L1 epilogue output h in the workspace */
 #define MOE_FLAG_TILE_128 2u       /* 128-wide GEMM tiles with double-buffered accumulators */
 #define MOE_FLAG_TILE_256 4u       /* 256-wide GEMM tiles (the default) */
+#define MOE_FLAG_CTA_PAIR 8u       /* always run the GEMMs on CTA pairs (256 x 256 tiles, BLOCK_M 256) */
+#define MOE_FLAG_CTA_SINGLE 16u    /* never run the GEMMs on CTA pairs */
 
 /* ---------------------------------------------------------------- config / plan */
 
@@ -112,8 +114,10 @@ int moe_plan_destroy(moe_plan_t plan);
 /*
  * BLOCK_M the routing pads each expert segment to for num_tokens tokens
  * (DeepGemmMegaMoEExperts.get_block_m; the pages' rule is inside a closed
- * library, ours is a constant 128: the MMA tile height). Deterministic in
- * (plan, num_tokens).
+ * library). Ours: 256 when the routed GEMMs run on CTA pairs (on average at
+ * least 192 routed rows per expert, num_tokens * top_k / num_experts, or
+ * MOE_FLAG_CTA_PAIR), else 128 (the MMA tile height of one CTA). Deterministic
+ * in (plan, num_tokens).
  */
 int moe_plan_block_m(moe_plan_t plan, int32_t num_tokens, int32_t* block_m);
 
@@ -294,6 +298,14 @@ int moe_plan_kernel_times(moe_plan_t plan, float* ms, int32_t count);
  */
 int moe_permute_noalloc(const int32_t* topk_ids, int32_t num_tokens, int32_t top_k, int32_t num_experts,
                         int32_t* inv_perm, int32_t* expert_offsets, void* stream);
+
+/*
+ * Limit of each bounded wait inside the GEMM kernels (default 2 s; 0 restores
+ * the default). A wait that runs out makes the kernel record MOE_ERR_TIMEOUT,
+ * wait for its own copies and MMAs, free its tensor memory and return, leaving
+ * the CUDA context usable; moe_last_status reports it. Used to test that path.
+ */
+int moe_plan_set_wait_timeout(moe_plan_t plan, uint64_t timeout_ns);
 
 /* Static string for a status code. */
 const char* moe_error_string(int32_t status);

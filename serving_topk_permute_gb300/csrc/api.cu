@@ -58,6 +58,25 @@ int validate(const moe_config_t* c) {
     return MOE_OK;
 }
 
+// ------------------------------------------------------------------ GEMM variant per call
+// Routed GEMMs run on CTA pairs (256 x 256 tiles, segments padded to 256 rows)
+// when experts get at least PAIR_MIN_ROWS routed rows on average, else on single
+// CTAs (128-row segments); the dense shared expert uses pairs from PAIR_MIN_ROWS
+// tokens. MOE_FLAG_CTA_PAIR / MOE_FLAG_CTA_SINGLE force either.
+constexpr int64_t PAIR_MIN_ROWS = 192;
+
+bool use_pair(const moe_config_t& c, int64_t rows_per_expert) {
+    if (c.flags & MOE_FLAG_CTA_SINGLE) return false;
+    if (c.flags & MOE_FLAG_CTA_PAIR) return true;
+    return rows_per_expert >= PAIR_MIN_ROWS;
+}
+
+int64_t routed_rows_per_expert(const moe_config_t& c, int T) {
+    return ceil_div((int64_t)T * c.top_k, c.num_experts);
+}
+
+int block_m_for(const moe_config_t& c, int T) { return use_pair(c, routed_rows_per_expert(c, T)) ? 2 * BM : BM; }
+
 // ------------------------------------------------------------------ workspace layout
 enum Region {
     R_ERR, R_META, R_CNT, R_OFF, R_TILE_EXPERT, R_SRC, R_INV, R_XSCALE, R_XQ, R_XSF, R_HQ, R_HSF, R_Y, R_HDBG,
@@ -75,10 +94,11 @@ Layout layout_of(const moe_config_t& c, int T) {
     Layout L{};
     const Dims d = dims_of(c);
     const int64_t R = (int64_t)T * d.k;
-    L.m_pad_max = align_up(R + (int64_t)d.E * (BM - 1), BM);
-    if (L.m_pad_max == 0) L.m_pad_max = BM;
+    const int bm = block_m_for(c, T);
+    L.m_pad_max = align_up(R + (int64_t)d.E * (bm - 1), bm);
+    if (L.m_pad_max == 0) L.m_pad_max = bm;
     L.m_tiles_max = L.m_pad_max / BM;
-    L.t_pad = align_up(T > 0 ? T : 1, BM);
+    L.t_pad = align_up(T > 0 ? T : 1, 2 * BM);
     const int S = fmt_sf_atoms(d.fmt);
     const int64_t nks_h = fmt_k_stages(d.fmt, d.H), nks_i = fmt_k_stages(d.fmt, d.I);
     int64_t sz[R_COUNT] = {};
@@ -205,7 +225,10 @@ int moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     if (!get_encode()) return MOE_ERR_CUDA;
     CUDA_TRY(route_prepare(MAX_EXPERTS));
-    for (int f = MOE_FMT_BF16; f <= MOE_FMT_NVFP4; ++f) CUDA_TRY(gemm_prepare(f));
+    for (int f = MOE_FMT_BF16; f <= MOE_FMT_NVFP4; ++f) {
+        CUDA_TRY(gemm_prepare(f));
+        CUDA_TRY(gemm2_prepare(f));
+    }
     CUDA_TRY(combine_prepare());
     moe_plan_s* p = new (std::nothrow) moe_plan_s;
     if (!p) return MOE_ERR_INVALID_ARG;
@@ -229,6 +252,12 @@ int moe_plan_enable_timing(moe_plan_t plan, int32_t enable) {
     return MOE_OK;
 }
 
+int moe_plan_set_wait_timeout(moe_plan_t plan, uint64_t timeout_ns) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    plan->timeout_ns = timeout_ns ? timeout_ns : DEFAULT_TIMEOUT_NS;
+    return MOE_OK;
+}
+
 int moe_plan_kernel_times(moe_plan_t plan, float* ms, int32_t count) {
     if (!plan || !ms || count < MOE_NUM_KERNELS || !plan->timing) return MOE_ERR_INVALID_ARG;
     for (int i = 0; i < MOE_NUM_KERNELS; ++i) {
@@ -248,7 +277,7 @@ int moe_plan_destroy(moe_plan_t plan) {
 
 int moe_plan_block_m(moe_plan_t plan, int32_t num_tokens, int32_t* block_m) {
     if (!plan || !block_m || num_tokens < 0) return MOE_ERR_INVALID_ARG;
-    *block_m = BM;
+    *block_m = block_m_for(plan->cfg, num_tokens);
     return MOE_OK;
 }
 
@@ -354,7 +383,8 @@ static int choose_bn(const moe_config_t& c, int64_t rows_per_expert) {
     return 256;
 }
 
-static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, int64_t rows_per_expert, const void* xq,
+// one expert MLP pass; m_tiles_* count 128-row tiles on single CTAs, 256-row tiles on pairs
+static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool pair, const void* xq,
                    const uint8_t* xsf, int64_t rows,
                    const moe_weights_t* w, const int* m_tiles_dev, int m_tiles_host, int64_t m_tiles_max,
                    const int* tile_expert, const int* src, int m_valid, const float* x_scale, const float* a2,
@@ -375,10 +405,19 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, int64_
     g.act_beta = activation ? c.act_beta : 0.0f;
     g.act_clamp = c.act_clamp;
     g.act_has_clamp = activation ? c.act_has_clamp : 0;
-    const int bn = choose_bn(c, rows_per_expert);
+    const int bn = pair ? 2 * BM : choose_bn(c, 0);
+    const uint32_t b_box = pair ? NBLK : bn;  // a CTA of a pair loads half of the 256 weight rows
+    auto launch = [&](bool l1, int64_t tiles) {
+        if (pair) {
+            const int grid = 2 * (int)std::min<int64_t>(p->num_sms / 2, std::max<int64_t>(1, tiles));
+            return launch_gemm2(fmt, l1, ta, tb, g, grid, st);
+        }
+        const int grid = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, tiles));
+        return launch_gemm(fmt, l1, bn, ta, tb, g, grid, st);
+    };
     // L1: [rows, H] x w13[e]^T -> h [rows, I]
     if (!map_2d(&ta, xq, fmt_row_bytes(fmt, H), rows, BM)) return MOE_ERR_CUDA;
-    if (!map_3d(&tb, w->w13, fmt_row_bytes(fmt, H), 2 * (uint64_t)I, E, bn)) return MOE_ERR_CUDA;
+    if (!map_3d(&tb, w->w13, fmt_row_bytes(fmt, H), 2 * (uint64_t)I, E, b_box)) return MOE_ERR_CUDA;
     g.sfa = xsf;
     g.sfb = (const uint8_t*)w->w13_sf;
     g.nks = (int)fmt_k_stages(fmt, H);
@@ -393,14 +432,13 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, int64_
     g.I = I;
     g.h_nks = (int)fmt_k_stages(fmt, I);
     g.h_debug = h_debug;
-    const int grid1 = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, m_tiles_max * g.n_tiles));
     {
         KernelTimer kt(p, kid1, st);
-        CUDA_TRY(launch_gemm(fmt, true, bn, ta, tb, g, grid1, st));
+        CUDA_TRY(launch(true, m_tiles_max * g.n_tiles));
     }
     // L2: h [rows, I] x w2[e]^T -> y [rows, H]
     if (!map_2d(&ta, hq, fmt_row_bytes(fmt, I), rows, BM)) return MOE_ERR_CUDA;
-    if (!map_3d(&tb, w->w2, fmt_row_bytes(fmt, I), H, E, bn)) return MOE_ERR_CUDA;
+    if (!map_3d(&tb, w->w2, fmt_row_bytes(fmt, I), H, E, b_box)) return MOE_ERR_CUDA;
     g.sfa = hsf;
     g.sfb = (const uint8_t*)w->w2_sf;
     g.nks = (int)fmt_k_stages(fmt, I);
@@ -410,10 +448,9 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, int64_
     g.gscale = w->w2_gs;
     g.y = y;
     g.ldy = H;
-    const int grid2 = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, m_tiles_max * g.n_tiles));
     {
         KernelTimer kt(p, kid1 + 1, st);
-        CUDA_TRY(launch_gemm(fmt, false, bn, ta, tb, g, grid2, st));
+        CUDA_TRY(launch(false, m_tiles_max * g.n_tiles));
     }
     return MOE_OK;
 }
@@ -444,12 +481,14 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
     auto R = [&](int r) { return ws + L.off[r]; };
     int* err = (int*)R(R_ERR);
     int* meta = (int*)R(R_META);
+    const bool routed_pair = use_pair(c, routed_rows_per_expert(c, T));
+    const int bm = routed_pair ? 2 * BM : BM;
     CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int), st));  // the status reflects this call only
     for (bool& r : plan->ran) r = false;
 
     {
         KernelTimer kt(plan, MOE_KERNEL_ROUTE, st);
-        CUDA_TRY(launch_route(topk_ids, T, d.k, d.E, BM, (int*)R(R_CNT), (int*)R(R_OFF), (int*)R(R_SRC), (int*)R(R_INV),
+        CUDA_TRY(launch_route(topk_ids, T, d.k, d.E, bm, (int*)R(R_CNT), (int*)R(R_OFF), (int*)R(R_SRC), (int*)R(R_INV),
                           (int*)R(R_TILE_EXPERT), meta, err, st));
     }
     DispatchArgs da{};
@@ -470,14 +509,16 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
         CUDA_TRY(launch_dispatch(da, st));
     }
 
-    int rc = run_mlp(plan, MOE_KERNEL_L1, d.fmt, d.E, d.I, d.H, ceil_div((int64_t)T * d.k, d.E), R(R_XQ), R(R_XSF), L.m_pad_max, weights, meta + 1, 0, L.m_tiles_max,
+    int rc = run_mlp(plan, MOE_KERNEL_L1, d.fmt, d.E, d.I, d.H, routed_pair, R(R_XQ), R(R_XSF), L.m_pad_max, weights,
+                     meta + 1, 0, L.m_pad_max / bm,
                      (const int*)R(R_TILE_EXPERT), (const int*)R(R_SRC), 0, (const float*)R(R_XSCALE), l2_act_scale,
                      R(R_HQ), R(R_HSF), (c.flags & MOE_FLAG_DEBUG_H) ? (float*)R(R_HDBG) : nullptr,
                      (__nv_bfloat16*)R(R_Y), err, true, st);
     if (rc != MOE_OK) return rc;
     if (d.Is > 0) {
-        const int tiles = (int)(L.t_pad / BM);
-        rc = run_mlp(plan, MOE_KERNEL_SHARED_L1, d.sfmt, 1, d.Is, d.H, T, R(R_SXQ), R(R_SXSF), L.t_pad, shared, nullptr, tiles, tiles, nullptr,
+        const bool shared_pair = use_pair(c, T);
+        const int tiles = (int)(L.t_pad / (shared_pair ? 2 * BM : BM));
+        rc = run_mlp(plan, MOE_KERNEL_SHARED_L1, d.sfmt, 1, d.Is, d.H, shared_pair, R(R_SXQ), R(R_SXSF), L.t_pad, shared, nullptr, tiles, tiles, nullptr,
                      nullptr, T, nullptr, nullptr, R(R_SHQ), R(R_SHSF), nullptr, (__nv_bfloat16*)R(R_SY), err, false,
                      st);
         if (rc != MOE_OK) return rc;

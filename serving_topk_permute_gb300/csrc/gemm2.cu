@@ -1,0 +1,320 @@
+// gemm2.cu -- the grouped GEMM on CTA pairs (tcgen05 cta_group::2), for expert
+// segments long enough to fill 256-row tiles (the prefill shapes and the dense
+// shared expert).
+//
+// A cluster of two CTAs on two SMs computes one 256 x 256 tile: each CTA stages
+// its own 128 A rows and one half (128 rows) of the 256 weight rows per K stage
+// (32 KB instead of 48 KB, so 5-6 stages fit instead of 4), plus the scale atoms
+// its tensor-memory copy needs (its A rows' atoms and both weight halves' atoms).
+// The leader CTA's MMA thread issues 256x256xK MMAs that read both CTAs' shared
+// memory and write each CTA's 128 accumulator rows into its own tensor memory,
+// and commits to the barriers of both CTAs at once. The follower's warp 1
+// forwards "stage landed" from its local barrier to the leader's; the follower's
+// epilogue warps report "accumulator read" to the leader the same way. Tiles are
+// walked row-tile-major and strided over the clusters. Every pipeline wait is
+// bounded; a CTA that gives up still waits for its own copies and MMAs.
+#include "gemm_epilogue.cuh"
+
+namespace moe {
+
+template <int FMT>
+struct Gemm2Cfg {
+    static constexpr int S = fmt_sf_atoms(FMT);
+    static constexpr int BN = 256;                      // weight rows per pair tile
+    static constexpr int NB = BN / NBLK;
+    static constexpr int STAGES = FMT == MOE_FMT_NVFP4 ? 5 : 6;
+    static constexpr int A_BYTES = BM * BK_BYTES;      // this CTA's 128 rows
+    static constexpr int B_BYTES = NBLK * BK_BYTES;    // this CTA's half of the weight rows
+    static constexpr int SFA_BYTES = S * ATOM_BYTES;
+    static constexpr int SFB_BYTES = S * NB * ATOM_BYTES;  // both halves: each CTA's MMA half needs all N
+    static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int STAGE_BYTES = (TX_BYTES + 1023) / 1024 * 1024;
+    static constexpr int ACC_COLS = BN;
+    static constexpr int SF_COLS = 4 * S * (1 + NB);
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static_assert(ACC_COLS + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+template <int FMT, bool L1>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    grouped_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const GemmArgs p) {
+    using C = Gemm2Cfg<FMT>;
+    constexpr int S = C::S, NB = C::NB, STAGES = C::STAGES, BN = C::BN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+    // barriers: full[STAGES], empty[STAGES], tfull, tempty, drain
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* never = reinterpret_cast<int*>(tmem_slot + 2);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t tfull_bar = bar0 + 8 * (2 * STAGES);
+    const uint32_t tempty_bar = tfull_bar + 8;
+    const uint32_t drain_bar = tfull_bar + 16;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar0 + 8 * s, leader ? 2 : 1);     // full: own loads (+ the follower's forward)
+            mbar_init(bar0 + 8 * (STAGES + s), 1);       // empty: the leader's commit
+        }
+        mbar_init(tfull_bar, 1);
+        mbar_init(tempty_bar, leader ? 2 * EPI_WARPS : EPI_WARPS);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        *never = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc2(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish2();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer's barriers exist before anyone arrives on them
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
+    const int m_tiles = p.m_tiles_dev ? *p.m_tiles_dev : p.m_tiles_host;  // 256-row tiles
+    const int total = m_tiles * p.n_tiles;
+
+    auto give_up = [&]() {
+        set_error(p.err, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int last_parity[STAGES];
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s) last_parity[s] = -1;
+            bool ok = true;
+            for (int tile = pair; ok && tile < total; tile += npairs) {
+                const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+                const int e = p.tile_expert ? p.tile_expert[mt] : 0;
+                const int a_tile = 2 * mt + (int)rank;  // this CTA's 128-row tile
+                for (int ks = 0; ks < p.nks; ++ks) {
+                    const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (STAGES + stage);
+                    if (!mbar_wait(empty, phase ^ 1, tmo, abort_flag)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = smem_u32(smem + stage * C::STAGE_BYTES);
+                    mbar_arrive_expect_tx(full, C::TX_BYTES);
+                    tma_load_2d(st, &tmA, full, ks * BK_BYTES, a_tile * BM);
+                    tma_load_3d(st + C::A_BYTES, &tmB, full, ks * BK_BYTES, nt * BN + (int)rank * NBLK, e);
+                    if constexpr (S > 0) {
+                        bulk_load(st + C::A_BYTES + C::B_BYTES,
+                                  p.sfa + ((int64_t)a_tile * p.nks + ks) * C::SFA_BYTES, C::SFA_BYTES, full);
+                        const int64_t blk = ((int64_t)e * p.nks + ks) * p.sf_blocks + (int64_t)nt * NB;
+                        bulk_load(st + C::A_BYTES + C::B_BYTES + C::SFA_BYTES, p.sfb + blk * S * ATOM_BYTES,
+                                  C::SFB_BYTES, full);
+                    }
+                    last_parity[stage] = (int)phase;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // every load this CTA issued lands before it may exit (the leader's full barrier
+            // also needs the follower's forward, so a leader that gave up may wait the limit)
+            for (int s = 0; s < STAGES; ++s)
+                if (last_parity[s] >= 0) mbar_wait(bar0 + 8 * s, (uint32_t)last_parity[s], DRAIN_TIMEOUT_NS, never);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            bool issued = false;
+            for (int tile = pair; ok && tile < total; tile += npairs) {
+                if (!mbar_wait_cl(tempty_bar, acc_phase ^ 1, tmo, abort_flag)) {
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+                for (int ks = 0; ks < p.nks; ++ks) {
+                    const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (STAGES + stage);
+                    if (!mbar_wait_cl(full, phase, tmo, abort_flag)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t sfa_col = tmem_base + C::ACC_COLS + stage * C::SF_COLS;
+                    const uint32_t sfb_col = sfa_col + 4 * S;
+                    if constexpr (S > 0) {
+                        const uint32_t sfa_smem = st + C::A_BYTES + C::B_BYTES;
+#pragma unroll
+                        for (int a = 0; a < S; ++a)
+                            tc_cp2_sf_atom(sfa_col + 4 * a, sf_atom_desc(sfa_smem + a * ATOM_BYTES));
+                        // shared memory holds the weight atoms as [block][s]; tensor memory wants [s][block]
+#pragma unroll
+                        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                            for (int a = 0; a < S; ++a)
+                                tc_cp2_sf_atom(sfb_col + 4 * (a * NB + nb),
+                                               sf_atom_desc(sfa_smem + C::SFA_BYTES + (nb * S + a) * ATOM_BYTES));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint64_t ad = kmajor_sw128_desc(st + j * 32);
+                        const uint64_t bd = kmajor_sw128_desc(st + C::A_BYTES + j * 32);
+                        const uint32_t accumulate = (ks > 0 || j > 0) ? 1u : 0u;
+                        if constexpr (FMT == MOE_FMT_BF16)
+                            mma2_bf16(tmem_base, ad, bd, idesc_m(idesc_bf16(BN), 2 * BM), accumulate);
+                        else if constexpr (FMT == MOE_FMT_MXFP8)
+                            mma2_mxf8(tmem_base, ad, bd, idesc_m(idesc_mxf8(BN, j), 2 * BM), sfa_col, sfb_col,
+                                      accumulate);
+                        else
+                            mma2_nvf4(tmem_base, ad, bd, idesc_m(idesc_nvf4(BN), 2 * BM), sfa_col + 4 * j,
+                                      sfb_col + 4 * NB * j, accumulate);
+                    }
+                    issued = true;
+                    tc_commit2_mc(empty, 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit2_mc(tfull_bar, 0x3);
+                acc_phase ^= 1;
+            }
+            // every MMA and copy issued completes before either CTA frees its tensor memory
+            if (issued) {
+                tc_commit2_mc(drain_bar, 0x1);
+                mbar_wait(drain_bar, 0, DRAIN_TIMEOUT_NS, never);
+            }
+        } else if (lane == 0) {
+            // follower: forward "stage landed" to the leader's full barrier, in stage order
+            const uint32_t leader_full0 = mapa_shared(bar0, 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < total; tile += npairs) {
+                for (int ks = 0; ks < p.nks; ++ks) {
+                    if (!mbar_wait(bar0 + 8 * stage, phase, tmo, abort_flag)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_cluster(leader_full0 + 8 * stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        }
+    } else {
+        const int q = warp % 4;
+        const int cg = (warp - 2) / 4;
+        const uint32_t leader_tempty = mapa_shared(tempty_bar, 0);
+        uint32_t acc_phase = 0;
+        for (int tile = pair; tile < total; tile += npairs) {
+            if (!mbar_wait(tfull_bar, acc_phase, tmo, abort_flag)) {
+                give_up();
+                break;
+            }
+            tc_fence_after();
+            const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+            const int e = p.tile_expert ? p.tile_expert[mt] : 0;
+            const int row = mt * 2 * BM + (int)rank * BM + q * 32 + lane;
+            const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16);
+            if constexpr (L1)
+                epilogue_l1<FMT, BN>(p, tacc, row, nt, e, cg);
+            else
+                epilogue_l2<FMT, BN>(p, tacc, row, nt, e, cg);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(tempty_bar);
+                else
+                    mbar_arrive_cluster(leader_tempty);
+            }
+            acc_phase ^= 1;
+        }
+    }
+    __syncthreads();
+    cluster_sync();  // both CTAs are done with each other's barriers and the MMAs have drained
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc2(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+template <int FMT, bool L1>
+static cudaError_t set_attr2() {
+    return cudaFuncSetAttribute(grouped_gemm2_kernel<FMT, L1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Gemm2Cfg<FMT>::SMEM);
+}
+
+cudaError_t gemm2_prepare(int fmt) {
+    cudaError_t e;
+    switch (fmt) {
+        case MOE_FMT_BF16:
+            if ((e = set_attr2<MOE_FMT_BF16, true>()) != cudaSuccess) return e;
+            return set_attr2<MOE_FMT_BF16, false>();
+        case MOE_FMT_MXFP8:
+            if ((e = set_attr2<MOE_FMT_MXFP8, true>()) != cudaSuccess) return e;
+            return set_attr2<MOE_FMT_MXFP8, false>();
+        default:
+            if ((e = set_attr2<MOE_FMT_NVFP4, true>()) != cudaSuccess) return e;
+            return set_attr2<MOE_FMT_NVFP4, false>();
+    }
+}
+
+template <int FMT, bool L1>
+static cudaError_t launch2_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
+                             cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Gemm2Cfg<FMT>::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, grouped_gemm2_kernel<FMT, L1>, tmA, tmB, a);
+}
+
+// grid: an even number of CTAs (pairs); the B tensor map's box is 128 rows (one half)
+cudaError_t launch_gemm2(int fmt, bool l1, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                         int grid, cudaStream_t st) {
+    if (grid % 2) return cudaErrorInvalidValue;
+    switch (fmt) {
+        case MOE_FMT_BF16:
+            return l1 ? launch2_t<MOE_FMT_BF16, true>(tmA, tmB, a, grid, st)
+                      : launch2_t<MOE_FMT_BF16, false>(tmA, tmB, a, grid, st);
+        case MOE_FMT_MXFP8:
+            return l1 ? launch2_t<MOE_FMT_MXFP8, true>(tmA, tmB, a, grid, st)
+                      : launch2_t<MOE_FMT_MXFP8, false>(tmA, tmB, a, grid, st);
+        default:
+            return l1 ? launch2_t<MOE_FMT_NVFP4, true>(tmA, tmB, a, grid, st)
+                      : launch2_t<MOE_FMT_NVFP4, false>(tmA, tmB, a, grid, st);
+    }
+}
+
+}  // namespace moe

@@ -24,7 +24,8 @@ W13, W13_SF, W2, W2_SF, SHARED_W13, SHARED_W13_SF, SHARED_W2, SHARED_W2_SF, W13_
 REGIONS = {"counts": 0, "offsets": 1, "src": 2, "inv_perm": 3, "xq": 4, "xsf": 5, "x_scale": 6, "hq": 7,
            "hsf": 8, "h_debug": 9, "y": 10, "meta": 11, "shared_y": 12}
 FLAG_DEBUG_H = 1
-FLAG_TILE = {0: 0, 128: 2, 256: 4}   # GEMM tile width: 0 = chosen by rows per expert
+FLAG_TILE = {0: 0, 128: 2, 256: 4}   # GEMM tile width: 0 = the library's choice
+FLAG_CTA = {"auto": 0, "pair": 8, "single": 16}   # GEMMs on CTA pairs: by rows per expert / always / never
 KERNELS = ["route", "dispatch", "l1", "l2", "shared_l1", "shared_l2", "combine"]
 
 
@@ -76,6 +77,7 @@ def lib() -> ctypes.CDLL:
             "moe_plan_enable_timing": [P, I32],
             "moe_plan_kernel_times": [P, P, I32],
             "moe_permute_noalloc": [P, I32, I32, I32, P, P, P],
+            "moe_plan_set_wait_timeout": [P, ctypes.c_uint64],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -144,13 +146,14 @@ class LayerConfig:
     norm_eps: float = 1e-6
     debug_h: bool = False
     tile: int = 0
+    cta: str = "auto"
 
     def to_c(self) -> Config:
         return Config(self.num_experts, self.hidden, self.inter, self.top_k, self.max_tokens, FORMATS[self.fmt], 0,
                       self.act_alpha, self.act_beta, 0.0 if self.act_clamp is None else self.act_clamp,
                       0 if self.act_clamp is None else 1, self.shared_inter, FORMATS[self.shared_fmt],
                       1 if self.post_norm else 0, self.norm_eps,
-                      (FLAG_DEBUG_H if self.debug_h else 0) | FLAG_TILE[self.tile])
+                      (FLAG_DEBUG_H if self.debug_h else 0) | FLAG_TILE[self.tile] | FLAG_CTA[self.cta])
 
 
 def validate(cfg: LayerConfig) -> int:
@@ -257,6 +260,10 @@ class Plan:
             ctypes.byref(sh) if sh is not None else None, _ptr(norm_gamma), _ptr(out), _ptr(workspace),
             workspace.numel(), _stream(stream)))
         return out
+
+    def set_wait_timeout(self, ns: int):
+        """Limit of each bounded wait in the GEMM kernels (0: the default, 2 s)."""
+        _check("moe_plan_set_wait_timeout", lib().moe_plan_set_wait_timeout(self._h, ns))
 
     def enable_timing(self, enable: bool = True):
         _check("moe_plan_enable_timing", lib().moe_plan_enable_timing(self._h, 1 if enable else 0))

@@ -62,7 +62,7 @@ def test_routing_and_dispatch_bit_exact_full_size(name):
     assert np.array_equal(G.region_i32(run, T, "src")[:M_pad], src)
     assert np.array_equal(G.region_i32(run, T, "inv_perm")[:T * k].reshape(T, k), inv)
     meta = G.region_i32(run, T, "meta")
-    assert meta[0] == M_pad and meta[1] == M_pad // 128
+    assert meta[0] == M_pad and meta[1] == M_pad // run.plan.block_m(T)
 
     # dispatch codes: every routed row holds its token's codes
     d = OM.dispatch_quantize(case.x, shape.fmt)
@@ -88,13 +88,14 @@ def test_routing_and_dispatch_bit_exact_full_size(name):
 
 # ----------------------------------------------------------------------------- outputs, reduced sizes, every element
 
-@pytest.mark.parametrize("tile", [128, 256])
+@pytest.mark.parametrize("mode", list(G.MODES))
 @pytest.mark.parametrize("name", list(REDUCED))
-def test_forward_matches_oracle_reduced(name, tile):
-    """Both GEMM tile widths (128: double-buffered accumulators; 256: one accumulator)."""
+def test_forward_matches_oracle_reduced(name, mode):
+    """Every GEMM variant: single CTA with 128-wide tiles (double-buffered accumulators) or
+    256-wide tiles, and CTA pairs (256 x 256 tiles over 256-row segments)."""
     shape = REDUCED[name]
     case = G.float_case(shape)
-    run = G.run_gpu(case, tile=tile)
+    run = G.run_gpu(case, **G.MODES[mode])
     G.assert_close(G.out_f64(run), G.oracle_out(case), shape.fmt, name)
     assert run.plan.last_status(run.workspace) == 0
 
@@ -209,16 +210,18 @@ def test_masked_slots_and_duplicates():
     G.assert_close(G.out_f64(G.run_gpu(case)), G.oracle_out(case), "mxfp8", "masked/dup")
 
 
+@pytest.mark.parametrize("cta", ["single", "pair"])
 @pytest.mark.parametrize("fmt", ["bf16", "nvfp4"])
-def test_all_tokens_one_expert(fmt):
+def test_all_tokens_one_expert(fmt, cta):
     shape = _small_case(fmt, T=300, k=1)
     ids = np.full((300, 1), 5, np.int32)
     w = np.ones((300, 1), np.float32)
     case = G.float_case(shape, ids=ids, w=w)
-    run = G.run_gpu(case)
+    run = G.run_gpu(case, cta=cta)
     G.assert_close(G.out_f64(run), G.oracle_out(case), fmt, "one expert")
     off = G.region_i32(run, 300, "offsets")[:9]
-    assert off.tolist() == [0, 0, 0, 0, 0, 0, 384, 384, 384]
+    pad = 384 if run.plan.block_m(300) == 128 else 512
+    assert off.tolist() == [0, 0, 0, 0, 0, 0, pad, pad, pad]
 
 
 def test_bad_expert_id_reports_status_and_is_masked():
@@ -264,12 +267,13 @@ def test_workspace_too_small():
     assert e.value.status == 4
 
 
+@pytest.mark.parametrize("cta", ["single", "pair"])
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
-def test_deterministic(fmt):
+def test_deterministic(fmt, cta):
     shape = _small_case(fmt, T=150, k=4, E=8)
     case = G.float_case(shape)
-    a = G.run_gpu(case).out.clone()
-    b = G.run_gpu(case).out.clone()
+    a = G.run_gpu(case, cta=cta).out.clone()
+    b = G.run_gpu(case, cta=cta).out.clone()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
@@ -331,3 +335,26 @@ def test_weight_transform_layout(fmt):
     assert np.array_equal(kw["w2_sf"], _expected_sf_atoms(ew.w2_sf, shape.H, shape.I, g, False, shape.I))
     if fmt == "nvfp4":
         assert np.array_equal(kw["w13_gs"], ew.w13_gs) and np.array_equal(kw["w2_gs"], ew.w2_gs)
+
+
+# ----------------------------------------------------------------------------- failure detection
+
+@pytest.mark.parametrize("cta", ["single", "pair"])
+def test_bounded_wait_timeout_reports_and_context_survives(cta):
+    """A 1 ns limit makes the GEMM's pipeline waits run out: the kernel records
+    MOE_ERR_TIMEOUT, waits for its own copies and MMAs, and returns. The status reads
+    back, and the same plan with the default limit then computes the same answer."""
+    shape = _small_case("mxfp8", T=256, H=2048, I=512, E=4, k=2)
+    case = G.float_case(shape)
+    run = G.run_gpu(case, cta=cta)
+    good = G.out_f64(run)
+    run.plan.set_wait_timeout(1)
+    run.plan.forward(run.inputs["hidden"], run.inputs["topk_ids"], run.inputs["topk_weights"], run.kweights,
+                     workspace=run.workspace)
+    assert run.plan.last_status(run.workspace) == 7
+    run.plan.set_wait_timeout(0)
+    out = run.plan.forward(run.inputs["hidden"], run.inputs["topk_ids"], run.inputs["topk_weights"], run.kweights,
+                           workspace=run.workspace)
+    torch.cuda.synchronize()
+    assert run.plan.last_status(run.workspace) == 0
+    assert np.array_equal(out.float().cpu().numpy(), good)
