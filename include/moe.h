@@ -58,8 +58,8 @@ extern "C" {
 #define MOE_FLAG_DEBUG_H  1u       /* also keep the fp32 L1 epilogue output h in the workspace */
 #define MOE_FLAG_TILE_128 2u       /* 128-wide GEMM tiles with double-buffered accumulators */
 #define MOE_FLAG_TILE_256 4u       /* 256-wide GEMM tiles (the default) */
-#define MOE_FLAG_CTA_PAIR 8u       /* always run the GEMMs on CTA pairs (256 x 256 tiles, BLOCK_M 256) */
-#define MOE_FLAG_CTA_SINGLE 16u    /* never run the GEMMs on CTA pairs */
+#define MOE_FLAG_CTA_PAIR 8u       /* run the GEMMs on CTA pairs (256 x 256 tiles, BLOCK_M 256) */
+#define MOE_FLAG_CTA_SINGLE 16u    /* run the GEMMs on single CTAs (the default) */
 
 /* ---------------------------------------------------------------- config / plan */
 
@@ -114,10 +114,8 @@ int moe_plan_destroy(moe_plan_t plan);
 /*
  * BLOCK_M the routing pads each expert segment to for num_tokens tokens
  * (DeepGemmMegaMoEExperts.get_block_m; the pages' rule is inside a closed
- * library). Ours: 256 when the routed GEMMs run on CTA pairs (on average at
- * least 192 routed rows per expert, num_tokens * top_k / num_experts, or
- * MOE_FLAG_CTA_PAIR), else 128 (the MMA tile height of one CTA). Deterministic
- * in (plan, num_tokens).
+ * library). Ours: 128, the MMA tile height of one CTA; 256 when the plan runs
+ * its GEMMs on CTA pairs (MOE_FLAG_CTA_PAIR). Deterministic in (plan, num_tokens).
  */
 int moe_plan_block_m(moe_plan_t plan, int32_t num_tokens, int32_t* block_m);
 

@@ -59,16 +59,15 @@ int validate(const moe_config_t* c) {
 }
 
 // ------------------------------------------------------------------ GEMM variant per call
-// Routed GEMMs run on CTA pairs (256 x 256 tiles, segments padded to 256 rows)
-// when experts get at least PAIR_MIN_ROWS routed rows on average, else on single
-// CTAs (128-row segments); the dense shared expert uses pairs from PAIR_MIN_ROWS
-// tokens. MOE_FLAG_CTA_PAIR / MOE_FLAG_CTA_SINGLE force either.
-constexpr int64_t PAIR_MIN_ROWS = 192;
-
+// The GEMMs run on CTA pairs (256 x 256 tiles, routed segments padded to 256 rows)
+// only with MOE_FLAG_CTA_PAIR. Measured on GB300, pairs match single CTAs on the
+// dense shared expert (0.127 vs 0.125 ms for its L1 at T=4096) and lose on routed
+// prefill (L1 2.35 vs 2.14 ms), where 256-row padding adds MMA work; so single
+// CTAs (128-row segments) are the default.
 bool use_pair(const moe_config_t& c, int64_t rows_per_expert) {
+    (void)rows_per_expert;
     if (c.flags & MOE_FLAG_CTA_SINGLE) return false;
-    if (c.flags & MOE_FLAG_CTA_PAIR) return true;
-    return rows_per_expert >= PAIR_MIN_ROWS;
+    return (c.flags & MOE_FLAG_CTA_PAIR) != 0;
 }
 
 int64_t routed_rows_per_expert(const moe_config_t& c, int T) {

@@ -103,11 +103,25 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// one bounded test of a barrier phase: the thread may suspend for at most hint_ns
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// a non-suspending test of a barrier phase
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -115,17 +129,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// limits below this are polled without suspending (a suspended try_wait may sleep longer)
+constexpr uint64_t SHORT_WAIT_NS = 1000000ull;
+
+// the longest single suspension inside a bounded wait
+__device__ __forceinline__ uint32_t wait_hint(uint64_t timeout_ns) {
+    return (uint32_t)(timeout_ns < 1000000ull ? timeout_ns : 1000000ull);
+}
+
 // Wait for the phase of `bar` with parity `parity` to complete, giving up after
 // timeout_ns (or as soon as *abort is set). Returns false on give-up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                           const volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+    const uint32_t hint = wait_hint(timeout_ns);
+    if (timeout_ns < SHORT_WAIT_NS) {
+        for (uint64_t i = 0; i < 32 * (1 + timeout_ns / 256); ++i)
+            if (mbar_test_wait(bar, parity)) return true;
+        return false;
+    }
+    if (mbar_try_wait(bar, parity, hint)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    // rounds of 32 polls: bounds the wait even where the global timer ticks coarsely
+    const uint64_t max_rounds = 1 + timeout_ns / 256;
+    for (uint64_t round = 0;; ++round) {
         for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_try_wait(bar, parity, hint)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > timeout_ns) return false;
+        if (round >= max_rounds || globaltimer_ns() - t0 > timeout_ns) return false;
     }
 }
 
@@ -289,11 +319,22 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait_cl(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -303,13 +344,21 @@ __device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) 
 // as mbar_wait, with cluster-scope acquire (arrivals from the peer CTA)
 __device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                              const volatile int* abort) {
-    if (mbar_try_wait_cl(bar, parity)) return true;
+    const uint32_t hint = wait_hint(timeout_ns);
+    if (timeout_ns < SHORT_WAIT_NS) {
+        for (uint64_t i = 0; i < 32 * (1 + timeout_ns / 256); ++i)
+            if (mbar_test_wait_cl(bar, parity)) return true;
+        return false;
+    }
+    if (mbar_try_wait_cl(bar, parity, hint)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    // rounds of 32 polls: bounds the wait even where the global timer ticks coarsely
+    const uint64_t max_rounds = 1 + timeout_ns / 256;
+    for (uint64_t round = 0;; ++round) {
         for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait_cl(bar, parity)) return true;
+            if (mbar_try_wait_cl(bar, parity, hint)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > timeout_ns) return false;
+        if (round >= max_rounds || globaltimer_ns() - t0 > timeout_ns) return false;
     }
 }
 // tensor memory of a CTA pair: issued by one warp in each of the two CTAs
