@@ -15,7 +15,10 @@
 //                  accumulating in tensor memory; commits free the stage
 //   warps 2..17    epilogue: 4 warps per tensor-memory lane quarter, each on a
 //                  quarter of the tile's columns; one accumulator row per thread
-//                  via tcgen05.ld.
+//                  via tcgen05.ld. A warp copies its share of the accumulator
+//                  (at most 64 fp32 per thread) into registers and releases it
+//                  before it computes and stores, so its work overlaps the MMAs
+//                  of the next tile even with a single accumulator buffer.
 //                  L1: alpha, SwiGLU (MegaMoEActivation), requantisation of h to
 //                  the L2 input format (bf16 / MXFP8 1x32 UE8M0 / NVFP4 1x16 E4M3
 //                  under the scalar L2 input scale). L2: alpha, bf16 row store.
@@ -222,13 +225,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const int e = p.tile_expert ? p.tile_expert[mt] : 0;
             const int row = mt * BM + q * 32 + lane;
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            // hand the accumulator back as soon as it sits in registers
+            const uint32_t tempty = tempty0 + 8 * acc;
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty);
+            };
             if constexpr (L1)
-                epilogue_l1<FMT, BN>(p, tacc, row, nt, e, cg);
+                epilogue_l1<FMT, BN>(p, tacc, row, nt, e, cg, release);
             else
-                epilogue_l2<FMT, BN>(p, tacc, row, nt, e, cg);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+                epilogue_l2<FMT, BN>(p, tacc, row, nt, e, cg, release);
             if (++acc == NUM_ACC) {
                 acc = 0;
                 acc_phase ^= 1;

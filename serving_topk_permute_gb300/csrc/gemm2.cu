@@ -237,18 +237,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const int e = p.tile_expert ? p.tile_expert[mt] : 0;
             const int row = mt * 2 * BM + (int)rank * BM + q * 32 + lane;
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16);
+            // hand the accumulator back as soon as it sits in registers
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader)
+                        mbar_arrive(tempty_bar);
+                    else
+                        mbar_arrive_cluster(leader_tempty);
+                }
+            };
             if constexpr (L1)
-                epilogue_l1<FMT, BN>(p, tacc, row, nt, e, cg);
+                epilogue_l1<FMT, BN>(p, tacc, row, nt, e, cg, release);
             else
-                epilogue_l2<FMT, BN>(p, tacc, row, nt, e, cg);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (leader)
-                    mbar_arrive(tempty_bar);
-                else
-                    mbar_arrive_cluster(leader_tempty);
-            }
+                epilogue_l2<FMT, BN>(p, tacc, row, nt, e, cg, release);
             acc_phase ^= 1;
         }
     }

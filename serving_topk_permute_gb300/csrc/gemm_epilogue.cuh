@@ -33,13 +33,22 @@ __device__ __forceinline__ bool row_valid(const GemmArgs& p, int row, int* token
     return row < p.m_valid;
 }
 
+// Every epilogue first copies its share of the accumulator into registers (64 fp32
+// per thread at most), then calls release() -- which hands the accumulator back to
+// the MMA issuer -- and only then computes and stores, so that work overlaps the
+// next tile's MMAs.
+
 // L1 epilogue, one 32-column chunk of h: chunk k of the tile takes gate columns
 // 128 (k/2) + 32 (k%2) and the up columns 64 to their right, and produces h columns
 // nt * BN/2 + 32 k .. + 31 (the w13 rows are interleaved by 64 in 128-row blocks).
-template <int FMT, int BN>
-__device__ __forceinline__ void epilogue_l1(const GemmArgs& p, uint32_t tacc, int row, int nt, int e, int cg) {
+template <int FMT, int BN, typename Release>
+__device__ __forceinline__ void epilogue_l1(const GemmArgs& p, uint32_t tacc, int row, int nt, int e, int cg,
+                                            Release release) {
     constexpr int CHUNKS = BN / 64;
-    if (cg >= CHUNKS) return;  // warp-uniform
+    if (cg >= CHUNKS) {  // warp-uniform: this column group has no chunk in narrow tiles
+        release();
+        return;
+    }
     int t;
     const bool valid = row_valid(p, row, &t);
     float alpha = 1.0f, a2 = 1.0f;
@@ -53,6 +62,7 @@ __device__ __forceinline__ void epilogue_l1(const GemmArgs& p, uint32_t tacc, in
     tmem_ld32(tacc + gcol, g);
     tmem_ld32(tacc + gcol + 64, u);
     tmem_ld_wait();
+    release();
     if (!valid) return;
     const int hc = nt * (BN / 2) + 32 * k;  // first h column of this chunk
     float h[32];
@@ -120,18 +130,23 @@ __device__ __forceinline__ void epilogue_l1(const GemmArgs& p, uint32_t tacc, in
 }
 
 // L2 epilogue: column group cg (0..3) stores output columns [cg BN/4, (cg+1) BN/4) of the tile
-template <int FMT, int BN>
-__device__ __forceinline__ void epilogue_l2(const GemmArgs& p, uint32_t tacc, int row, int nt, int e, int cg) {
+template <int FMT, int BN, typename Release>
+__device__ __forceinline__ void epilogue_l2(const GemmArgs& p, uint32_t tacc, int row, int nt, int e, int cg,
+                                            Release release) {
     int t;
     const bool valid = row_valid(p, row, &t);
     float alpha = 1.0f;
     if constexpr (FMT == MOE_FMT_NVFP4) alpha = p.gscale[e] * (*p.a2);
     constexpr int PER = BN / 128;  // 32-column chunks per group
-#pragma unroll 1
-    for (int c = PER * cg; c < PER * cg + PER; ++c) {
-        float v[32];
-        tmem_ld32(tacc + c * 32, v);
-        tmem_ld_wait();
+    float vv[PER][32];
+#pragma unroll
+    for (int c = 0; c < PER; ++c) tmem_ld32(tacc + (PER * cg + c) * 32, vv[c]);
+    tmem_ld_wait();
+    release();
+#pragma unroll
+    for (int cc = 0; cc < PER; ++cc) {
+        const float(&v)[32] = vv[cc];
+        const int c = PER * cg + cc;
         const int col = nt * BN + c * 32;
         if (!valid || col >= p.N) continue;
         uint4* dst = reinterpret_cast<uint4*>(p.y + (int64_t)row * p.ldy + col);
