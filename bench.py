@@ -40,14 +40,17 @@ TENSOR_RATIO = {"bf16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0}
 ELEM_BYTES = {"bf16": 2.0, "mxfp8": 1.0, "nvfp4": 0.5}
 SF_PER_ELEM = {"bf16": 0.0, "mxfp8": 1.0 / 32, "nvfp4": 1.0 / 16}
 # DRAM bytes (read + write) per launch from one ncu capture of the current kernels
-# (profiles/grouped_gemm_*.md); an entry must be removed when its kernel changes
+# (profiles/grouped_gemm_*.md); an entry must be removed when its kernel changes. The
+# nvfp4_decode entries come from a capture at E=64 scaled by touched experts (249 / 64).
 NCU_TRAFFIC = {
-    ("mxfp8_small", "l1"): (225.152768e6 + 4.943360e6, "profiles/grouped_gemm_mxfp8_small.md"),
-    ("mxfp8_small", "l2"): (110.385408e6 + 3.610624e6, "profiles/grouped_gemm_mxfp8_small.md"),
-    ("nvfp4_decode", "l1"): (4.247895e9 + 4.720384e6, "profiles/grouped_gemm_nvfp4_decode.md"),
-    ("nvfp4_decode", "l2"): (2.093047e9 + 17.182464e6, "profiles/grouped_gemm_nvfp4_decode.md"),
+    ("mxfp8_small", "l1"): (225.204992e6 + 4.299776e6, "profiles/grouped_gemm_mxfp8_small.md"),
+    ("mxfp8_small", "l2"): (110.422272e6 + 3.370240e6, "profiles/grouped_gemm_mxfp8_small.md"),
+    ("nvfp4_decode", "l1"): ((1.092222e9 + 4.526592e6) * 249 / 64,
+                             "profiles/grouped_gemm_nvfp4_decode_e64.md (E=64, scaled by 249/64 touched experts)"),
+    ("nvfp4_decode", "l2"): ((0.538017e9 + 14.084352e6) * 249 / 64,
+                             "profiles/grouped_gemm_nvfp4_decode_e64.md (E=64, scaled by 249/64 touched experts)"),
 }
-# tokens the CPU oracle processes per timed sample (about 10-30 s of host work)
+# tokens of one reference-arm step, and of the first (sizing) call of cpu_baseline
 CPU_SAMPLE_TOKENS = {"bf16_toy": 64, "mxfp8_small": 24, "nvfp4_decode": 3, "mxfp8_prefill_zipf": 12,
                      "nvfp4_shared_norm": 6}
 
@@ -194,29 +197,54 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
 
-def oracle_sample(shape: S.MoeShape, seed: int, n_tokens: int):
-    """Time the CPU oracle on the first n_tokens tokens of the workload (recipe-B weights of the experts
-    those tokens touch). Returns (seconds, tokens, cores)."""
-    from oracle import moe as OM
-    x = S.hidden_states(shape, seed)
-    ids, w = S.router(shape, seed)
-    toks = list(range(min(n_tokens, shape.T)))
-    touched = sorted(set(int(e) for e in ids[toks].reshape(-1)))
-    ck = S.routed_code_checkpoint(shape, seed, experts=touched)
-    layer = OM.Layer(shape.E, shape.k, OM.ExpertWeights(ck.fmt, ck.w13, ck.w2, ck.w13_sf, ck.w2_sf, ck.w13_gs,
-                                                         ck.w2_gs))
-    if shape.fmt == "nvfp4":
-        layer.a2 = OM.l2_activation_scale(ck.w2_input_scale)
-    if shape.shared_I:
-        sc = S.shared_code_checkpoint(shape, seed)
-        layer.shared = OM.ExpertWeights(sc.fmt, sc.w13, sc.w2, sc.w13_sf, sc.w2_sf)
-    if shape.post_norm:
-        layer.norm_gamma = S.norm_gamma(shape, seed)
-        layer.norm_eps = shape.norm_eps
-    t0 = time.perf_counter()
-    OM.forward(layer, x, ids, w, tokens=toks)
-    dt = time.perf_counter() - t0
-    return dt, len(toks), blas_threads()
+class OracleSample:
+    """The CPU oracle on the first n tokens of a workload, with recipe-B weights of the experts those
+    tokens touch (generated once per sample size, outside the timed call)."""
+
+    def __init__(self, shape: S.MoeShape, seed: int = 0):
+        self.shape, self.seed = shape, seed
+        self.x = S.hidden_states(shape, seed)
+        self.ids, self.w = S.router(shape, seed)
+        self.layer, self.n_built = None, 0
+
+    def _build(self, n: int):
+        from oracle import moe as OM
+        shape, seed = self.shape, self.seed
+        touched = sorted(set(int(e) for e in self.ids[:n].reshape(-1)))
+        ck = S.routed_code_checkpoint(shape, seed, experts=touched)
+        layer = OM.Layer(shape.E, shape.k, OM.ExpertWeights(ck.fmt, ck.w13, ck.w2, ck.w13_sf, ck.w2_sf,
+                                                             ck.w13_gs, ck.w2_gs))
+        if shape.fmt == "nvfp4":
+            layer.a2 = OM.l2_activation_scale(ck.w2_input_scale)
+        if shape.shared_I:
+            sc = S.shared_code_checkpoint(shape, seed)
+            layer.shared = OM.ExpertWeights(sc.fmt, sc.w13, sc.w2, sc.w13_sf, sc.w2_sf)
+        if shape.post_norm:
+            layer.norm_gamma = S.norm_gamma(shape, seed)
+            layer.norm_eps = shape.norm_eps
+        self.layer, self.n_built = layer, n
+
+    def time(self, n: int) -> float:
+        """Seconds of one oracle forward over tokens [0, n)."""
+        from oracle import moe as OM
+        n = max(1, min(n, self.shape.T))
+        if n > self.n_built:
+            self._build(n)
+        t0 = time.perf_counter()
+        OM.forward(self.layer, self.x, self.ids, self.w, tokens=list(range(n)))
+        return time.perf_counter() - t0
+
+
+def oracle_baseline(shape: S.MoeShape, target_s: float = 12.0):
+    """cpu_baseline: a first timed call on CPU_SAMPLE_TOKENS tokens sizes a second one to about target_s
+    seconds of host work (at most the whole batch); the second one is reported."""
+    smp = OracleSample(shape)
+    n0 = min(CPU_SAMPLE_TOKENS[shape.name.split("+")[0]], shape.T)
+    dt0 = smp.time(n0)
+    n1 = max(n0, min(shape.T, int(n0 * target_s / max(dt0, 1e-3))))
+    if n1 == n0:
+        return dt0, n0, blas_threads()
+    return smp.time(n1), n1, blas_threads()
 
 
 def blas_threads() -> int:
@@ -237,14 +265,14 @@ def run_reference(args, shape: S.MoeShape):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    n_tok = CPU_SAMPLE_TOKENS[shape.name.split("+")[0]]
-    if args.warmup > 0:
-        oracle_sample(shape, 0, 1)
-    total_s, total_tok, cores = 0.0, 0, 1
+    n_tok = min(CPU_SAMPLE_TOKENS[shape.name.split("+")[0]], shape.T)
+    smp = OracleSample(shape)
+    for _ in range(args.warmup):
+        smp.time(1)
+    total_s, total_tok, cores = 0.0, 0, blas_threads()
     for i in range(args.steps):
-        dt, nt, cores = oracle_sample(shape, 0, n_tok)
-        total_s += dt
-        total_tok += nt
+        total_s += smp.time(n_tok)
+        total_tok += n_tok
     value = total_tok / total_s
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
@@ -345,14 +373,34 @@ def run_ours(args, shape: S.MoeShape):
     total_ms = reduce_max(sum(step_ms))
     value = world * T * args.steps / (total_ms / 1e3)
 
-    # ---- per-kernel times (library events around each launch, same stream, L2 flushed before each step)
+    # ---- per-kernel times: the library's events around each launch (same stream), recorded inside a
+    # CUDA graph of one forward so that no host launch gap falls between an event and its kernel; L2
+    # flushed before each step as above. If events in a graph cannot be timed, plain launches behind a
+    # spin kernel (the host enqueues the whole forward while it runs) stand in.
     plan.enable_timing(True)
     ktimes = {}
-    for i in range(min(args.steps, 200)):
-        flush.fill_(i & 0xFF)
-        step()
-        for k_, v in plan.kernel_times().items():
-            ktimes.setdefault(k_, []).append(v)
+    kernel_timing = "library events inside a CUDA graph of one forward"
+    try:
+        tgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tgraph):
+            step()
+        torch.cuda.synchronize()
+        for i in range(min(args.steps, 200)):
+            flush.fill_(i & 0xFF)
+            tgraph.replay()
+            for k_, v in plan.kernel_times().items():
+                ktimes.setdefault(k_, []).append(v)
+        del tgraph
+    except (pkg.MoeError, RuntimeError):
+        torch.cuda.synchronize()
+        ktimes = {}
+        kernel_timing = "library events around plain launches queued behind a spin kernel"
+        for i in range(min(args.steps, 200)):
+            flush.fill_(i & 0xFF)
+            torch.cuda._sleep(2_000_000)
+            step()
+            for k_, v in plan.kernel_times().items():
+                ktimes.setdefault(k_, []).append(v)
     plan.enable_timing(False)
 
     # ---- end to end: pinned host inputs -> device -> forward -> host output, every step
@@ -398,8 +446,7 @@ def run_ours(args, shape: S.MoeShape):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        n_tok = CPU_SAMPLE_TOKENS[shape.name.split("+")[0]]
-        dt, nt, cores = oracle_sample(shape, 0, n_tok)
+        dt, nt, cores = oracle_baseline(shape)
         cpu = {"value": round(nt / dt, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"first {nt} tokens of {shape.name} (NumPy fp64 oracle, {dt:.1f} s)"}
 
@@ -417,7 +464,8 @@ def run_ours(args, shape: S.MoeShape):
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": kernels_per_step * args.steps,
-        "timing": "value: CUDA-graph replays of one moe_forward, events per step; e2e: plain C-ABI calls",
+        "timing": "value: CUDA-graph replays of one moe_forward, events per step; e2e: plain C-ABI calls; "
+                  "per-kernel: " + kernel_timing,
         "clocks": clk,
         "wall_s": round(wall, 3),
     }
@@ -430,8 +478,9 @@ def run_ours(args, shape: S.MoeShape):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 2000; 10 for --impl reference, whose steps take seconds)")
+    ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (default 10; 3 for --impl reference)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=S.WORKLOAD_ORDER, default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -442,6 +491,11 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, help="profiling only: override the workload's T")
     ap.add_argument("--experts", type=int, help="profiling only: override the workload's E")
     args = ap.parse_args(argv)
+    ref = args.impl == "reference"
+    if args.steps is None:
+        args.steps = 10 if ref else 2000
+    if args.warmup is None:
+        args.warmup = 3 if ref else 10
     shape = S.WORKLOADS[args.workload]
     over = {k: v for k, v in (("T", args.tokens), ("E", args.experts)) if v}
     if over:
