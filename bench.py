@@ -4,7 +4,8 @@
 One step = one moe_forward over one batch of synthetic tokens: routing,
 dispatch quantisation, L1 GEMM (+SwiGLU, requant), L2 GEMM, [shared expert],
 combine [+RMSNorm]. Inputs are resident in HBM when the timed region starts;
-the L2 cache is flushed (a 256 MB write) before every timed step, outside the
+the L2 cache is flushed before every timed step (a 256 MB write, then a 256 MB read
+so that no dirty line of the flush is written back inside the step), outside the
 step's own events. Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
@@ -292,7 +293,7 @@ def workload_config(shape: S.MoeShape, world: int) -> dict:
             "format": shape.fmt, "shared_I": shape.shared_I, "shared_format": shape.shared_fmt if shape.shared_I
             else None, "post_norm": shape.post_norm, "global_batch": shape.T * world,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "l2": "flushed before every timed step (256 MB write)"}
+            "l2": "flushed before every timed step (256 MB write, then 256 MB read)"}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -316,7 +317,7 @@ def run_ours(args, shape: S.MoeShape):
     T = shape.T
     plan = pkg.Plan(pkg.LayerConfig(shape.E, shape.H, shape.I, shape.k, T, shape.fmt, shared_inter=shape.shared_I,
                                     shared_fmt=shape.shared_fmt, post_norm=shape.post_norm,
-                                    norm_eps=shape.norm_eps, tile=args.tile, cta=args.cta))
+                                    norm_eps=shape.norm_eps, tile=args.tile, cta=args.cta, serial=args.serial))
     ck = S.torch_code_checkpoint(shape, seed, dev)
     kw = plan.transform_weights({k: v for k, v in ck.items() if k != "w2_input_scale"})
     ks = plan.transform_shared_weights(S.torch_code_checkpoint(shape, seed, dev, shared=True)) \
@@ -330,7 +331,15 @@ def run_ours(args, shape: S.MoeShape):
     tw = torch.from_numpy(w).to(dev)
     out = torch.empty_like(hidden)
     ws = plan.alloc_workspace(T, dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush(i: int):
+        """Evict the L2: overwrite 256 MB, then read another 256 MB so that the written lines are
+        cleaned (written back) here rather than inside the next step."""
+        flush_w.fill_(i & 0xFF)
+        if not args.flush_write_only:
+            torch.amax(flush_r)
     torch.cuda.synchronize()
 
     def step():
@@ -361,7 +370,7 @@ def run_ours(args, shape: S.MoeShape):
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         evs[i][0].record()
         graph.replay()
         evs[i][1].record()
@@ -373,34 +382,18 @@ def run_ours(args, shape: S.MoeShape):
     total_ms = reduce_max(sum(step_ms))
     value = world * T * args.steps / (total_ms / 1e3)
 
-    # ---- per-kernel times: the library's events around each launch (same stream), recorded inside a
-    # CUDA graph of one forward so that no host launch gap falls between an event and its kernel; L2
-    # flushed before each step as above. If events in a graph cannot be timed, plain launches behind a
-    # spin kernel (the host enqueues the whole forward while it runs) stand in.
+    # ---- per-kernel times: the library's events around each launch (same stream), L2 flushed before each
+    # step as above. A spin kernel ahead of each forward lets the host queue the whole forward before the
+    # GPU reaches it, so no host launch gap falls between an event and its kernel.
     plan.enable_timing(True)
     ktimes = {}
-    kernel_timing = "library events inside a CUDA graph of one forward"
-    try:
-        tgraph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(tgraph):
-            step()
-        torch.cuda.synchronize()
-        for i in range(min(args.steps, 200)):
-            flush.fill_(i & 0xFF)
-            tgraph.replay()
-            for k_, v in plan.kernel_times().items():
-                ktimes.setdefault(k_, []).append(v)
-        del tgraph
-    except (pkg.MoeError, RuntimeError):
-        torch.cuda.synchronize()
-        ktimes = {}
-        kernel_timing = "library events around plain launches queued behind a spin kernel"
-        for i in range(min(args.steps, 200)):
-            flush.fill_(i & 0xFF)
-            torch.cuda._sleep(2_000_000)
-            step()
-            for k_, v in plan.kernel_times().items():
-                ktimes.setdefault(k_, []).append(v)
+    kernel_timing = "library events around plain launches queued behind a spin kernel"
+    for i in range(min(args.steps, 200)):
+        flush(i)
+        torch.cuda._sleep(1_000_000)
+        step()
+        for k_, v in plan.kernel_times().items():
+            ktimes.setdefault(k_, []).append(v)
     plan.enable_timing(False)
 
     # ---- end to end: pinned host inputs -> device -> forward -> host output, every step
@@ -412,7 +405,7 @@ def run_ours(args, shape: S.MoeShape):
     barrier()
     torch.cuda.synchronize()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         e2e_ev[i][0].record()
         hidden.view(torch.int16).copy_(h_hidden, non_blocking=True)
         tid.copy_(h_ids, non_blocking=True)
@@ -455,7 +448,9 @@ def run_ours(args, shape: S.MoeShape):
         "warmup": args.warmup, "ms_per_step": round(sum(step_ms) / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": shape.fmt if shape.fmt != "bf16" else "bf16",
         "data": "synthetic (seeded activations and routing; checkpoint bytes drawn on the device)",
-        "config": workload_config(shape, world),
+        "config": {**workload_config(shape, world), "launch": "serial" if args.serial else "programmatic dependent launch",
+                   "tile": args.tile or "library", "cta": args.cta,
+                   **({"l2": "flushed before every timed step (256 MB write only)"} if args.flush_write_only else {})},
         "roofline": rl,
         "layer": {"tflops": round(work["flops"] / sec / 1e12, 2), "hbm_gbs": round(work["bytes"] / sec / 1e9, 1),
                   "algorithmic_flops": work["flops"], "algorithmic_bytes": int(work["bytes"]),
@@ -488,6 +483,10 @@ def main(argv=None):
                     help="GEMM tile width (0: the library's choice by rows per expert)")
     ap.add_argument("--cta", choices=["auto", "pair", "single"], default="auto",
                     help="GEMMs on CTA pairs: the library's choice, always or never")
+    ap.add_argument("--flush-write-only", action="store_true",
+                    help="flush the L2 with the 256 MB write alone (its dirty lines are written back inside the step)")
+    ap.add_argument("--serial", action="store_true",
+                    help="launch each kernel after the previous one finishes (no programmatic dependent launch)")
     ap.add_argument("--tokens", type=int, help="profiling only: override the workload's T")
     ap.add_argument("--experts", type=int, help="profiling only: override the workload's E")
     args = ap.parse_args(argv)

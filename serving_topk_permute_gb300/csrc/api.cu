@@ -181,6 +181,7 @@ struct moe_plan_s {
     int num_sms;
     unsigned long long timeout_ns;
     bool timing = false;
+    bool pdl = true;  // programmatic dependent launch between the forward's kernels
     cudaEvent_t ev[2 * MOE_NUM_KERNELS] = {};
     bool ran[MOE_NUM_KERNELS] = {};
 };
@@ -203,9 +204,14 @@ struct KernelTimer {
 };
 }  // namespace
 
-#define CUDA_TRY(x)                              \
-    do {                                         \
-        if ((x) != cudaSuccess) return MOE_ERR_CUDA; \
+// a failed runtime call is reported as MOE_ERR_CUDA and cleared from the runtime's
+// last-error state, so that it does not surface in the caller's next CUDA call
+#define CUDA_TRY(x)                      \
+    do {                                 \
+        if ((x) != cudaSuccess) {        \
+            (void)cudaGetLastError();    \
+            return MOE_ERR_CUDA;         \
+        }                                \
     } while (0)
 
 extern "C" {
@@ -235,6 +241,7 @@ int moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     p->device = dev;
     p->num_sms = sms;
     p->timeout_ns = DEFAULT_TIMEOUT_NS;
+    p->pdl = (cfg->flags & MOE_FLAG_SERIAL) == 0;
     *out = p;
     return MOE_OK;
 }
@@ -409,10 +416,10 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool p
     auto launch = [&](bool l1, int64_t tiles) {
         if (pair) {
             const int grid = 2 * (int)std::min<int64_t>(p->num_sms / 2, std::max<int64_t>(1, tiles));
-            return launch_gemm2(fmt, l1, ta, tb, g, grid, st);
+            return launch_gemm2(fmt, l1, ta, tb, g, grid, st, p->pdl);
         }
         const int grid = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, tiles));
-        return launch_gemm(fmt, l1, bn, ta, tb, g, grid, st);
+        return launch_gemm(fmt, l1, bn, ta, tb, g, grid, st, p->pdl);
     };
     // L1: [rows, H] x w13[e]^T -> h [rows, I]
     if (!map_2d(&ta, xq, fmt_row_bytes(fmt, H), rows, BM)) return MOE_ERR_CUDA;
@@ -482,13 +489,12 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
     int* meta = (int*)R(R_META);
     const bool routed_pair = use_pair(c, routed_rows_per_expert(c, T));
     const int bm = routed_pair ? 2 * BM : BM;
-    CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int), st));  // the status reflects this call only
-    for (bool& r : plan->ran) r = false;
+    for (bool& r : plan->ran) r = false;  // the routing kernel zeroes the error word first
 
     {
         KernelTimer kt(plan, MOE_KERNEL_ROUTE, st);
         CUDA_TRY(launch_route(topk_ids, T, d.k, d.E, bm, (int*)R(R_CNT), (int*)R(R_OFF), (int*)R(R_SRC), (int*)R(R_INV),
-                          (int*)R(R_TILE_EXPERT), meta, err, st));
+                          (int*)R(R_TILE_EXPERT), meta, err, st, plan->pdl));
     }
     DispatchArgs da{};
     da.x = (const uint16_t*)hidden;
@@ -505,7 +511,7 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
     da.sxsf = R(R_SXSF);
     {
         KernelTimer kt(plan, MOE_KERNEL_DISPATCH, st);
-        CUDA_TRY(launch_dispatch(da, st));
+        CUDA_TRY(launch_dispatch(da, st, plan->pdl));
     }
 
     int rc = run_mlp(plan, MOE_KERNEL_L1, d.fmt, d.E, d.I, d.H, routed_pair, R(R_XQ), R(R_XSF), L.m_pad_max, weights,
@@ -535,7 +541,7 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
     ca.out = (__nv_bfloat16*)out;
     {
         KernelTimer kt(plan, MOE_KERNEL_COMBINE, st);
-        CUDA_TRY(launch_combine(ca, st));
+        CUDA_TRY(launch_combine(ca, st, plan->pdl));
     }
     return MOE_OK;
 }

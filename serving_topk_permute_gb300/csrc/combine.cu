@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 4) combine_kernel(const Combi
     __shared__ int s_rows[32];
     __shared__ float s_w[32];
     __shared__ float s_red[COMBINE_THREADS / 32];
+    grid_dep_wait();  // the L2 GEMM (and the shared expert) have written y
+    grid_dep_launch();
     if (tid < a.k) {
         s_rows[tid] = a.inv[(int64_t)t * a.k + tid];
         s_w[tid] = a.w[(int64_t)t * a.k + tid];
@@ -105,10 +107,11 @@ cudaError_t combine_prepare() {
     return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 4);
 }
 
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl) {
     const size_t smem = a.gamma ? (size_t)a.H * sizeof(float) : 0;
-    combine_kernel<<<a.T, COMBINE_THREADS, smem, st>>>(a);
-    return cudaGetLastError();
+    LaunchAttrs at(pdl);
+    cudaLaunchConfig_t cfg = at.config(dim3(a.T), dim3(COMBINE_THREADS), smem, st);
+    return cudaLaunchKernelEx(&cfg, combine_kernel, a);
 }
 
 }  // namespace moe

@@ -75,6 +75,16 @@ __device__ inline void set_error(int* err, int code) {
     if (err) atomicCAS(err, 0, code);
 }
 
+// Programmatic dependent launch. A kernel launched with the programmatic-serialisation
+// attribute may start while its predecessor in the stream is still running: it does
+// its set-up (shared memory, barriers, tensor memory), then grid_dep_wait() blocks
+// until the predecessor grid has completed and its writes are visible. Every global
+// read or write of the forward's buffers comes after that wait. grid_dep_launch()
+// then lets the successor start its own set-up. A kernel launched without the
+// attribute returns from both at once.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

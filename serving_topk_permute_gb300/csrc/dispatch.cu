@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
     __shared__ int s_rows[32];
     __shared__ float s_amax[DISPATCH_THREADS / 32];
 
+    grid_dep_wait();  // routing has written inv
+    grid_dep_launch();
     if (tid < a.k) s_rows[tid] = a.inv[(int64_t)t * a.k + tid];
 
     // load the token's row into registers
@@ -162,9 +164,10 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
     }
 }
 
-cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st) {
-    dispatch_kernel<<<a.T, DISPATCH_THREADS, 0, st>>>(a);
-    return cudaGetLastError();
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl) {
+    LaunchAttrs at(pdl);
+    cudaLaunchConfig_t cfg = at.config(dim3(a.T), dim3(DISPATCH_THREADS), 0, st);
+    return cudaLaunchKernelEx(&cfg, dispatch_kernel, a);
 }
 
 }  // namespace moe

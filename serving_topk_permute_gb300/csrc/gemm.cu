@@ -96,6 +96,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    grid_dep_wait();  // the set-up above overlaps the previous kernel; everything below reads its output
+    grid_dep_launch();
 
     const int m_tiles = p.m_tiles_dev ? *p.m_tiles_dev : p.m_tiles_host;
     const int total = m_tiles * p.n_tiles;
@@ -275,26 +277,29 @@ cudaError_t gemm_prepare(int fmt) {
 
 template <int FMT, bool L1, int BN>
 static cudaError_t launch_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                            cudaStream_t st) {
-    grouped_gemm_kernel<FMT, L1, BN><<<grid, GEMM_THREADS, GemmCfg<FMT, BN>::SMEM, st>>>(tmA, tmB, a);
-    return cudaGetLastError();
+                            cudaStream_t st, bool pdl) {
+    LaunchAttrs at(pdl);
+    cudaLaunchConfig_t cfg = at.config(dim3(grid), dim3(GEMM_THREADS), GemmCfg<FMT, BN>::SMEM, st);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<FMT, L1, BN>, tmA, tmB, a);
 }
 
 template <int FMT>
 static cudaError_t launch_fmt(bool l1, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                              int grid, cudaStream_t st) {
+                              int grid, cudaStream_t st, bool pdl) {
     if (bn == 128)
-        return l1 ? launch_t<FMT, true, 128>(tmA, tmB, a, grid, st) : launch_t<FMT, false, 128>(tmA, tmB, a, grid, st);
-    return l1 ? launch_t<FMT, true, 256>(tmA, tmB, a, grid, st) : launch_t<FMT, false, 256>(tmA, tmB, a, grid, st);
+        return l1 ? launch_t<FMT, true, 128>(tmA, tmB, a, grid, st, pdl)
+                  : launch_t<FMT, false, 128>(tmA, tmB, a, grid, st, pdl);
+    return l1 ? launch_t<FMT, true, 256>(tmA, tmB, a, grid, st, pdl)
+              : launch_t<FMT, false, 256>(tmA, tmB, a, grid, st, pdl);
 }
 
 cudaError_t launch_gemm(int fmt, bool l1, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                        int grid, cudaStream_t st) {
+                        int grid, cudaStream_t st, bool pdl) {
     if (bn != 128 && bn != 256) return cudaErrorInvalidValue;
     switch (fmt) {
-        case MOE_FMT_BF16: return launch_fmt<MOE_FMT_BF16>(l1, bn, tmA, tmB, a, grid, st);
-        case MOE_FMT_MXFP8: return launch_fmt<MOE_FMT_MXFP8>(l1, bn, tmA, tmB, a, grid, st);
-        default: return launch_fmt<MOE_FMT_NVFP4>(l1, bn, tmA, tmB, a, grid, st);
+        case MOE_FMT_BF16: return launch_fmt<MOE_FMT_BF16>(l1, bn, tmA, tmB, a, grid, st, pdl);
+        case MOE_FMT_MXFP8: return launch_fmt<MOE_FMT_MXFP8>(l1, bn, tmA, tmB, a, grid, st, pdl);
+        default: return launch_fmt<MOE_FMT_NVFP4>(l1, bn, tmA, tmB, a, grid, st, pdl);
     }
 }
 

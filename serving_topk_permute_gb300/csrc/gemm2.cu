@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     cluster_sync();  // the peer's barriers exist before anyone arrives on them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    grid_dep_wait();  // the set-up above overlaps the previous kernel; everything below reads its output
+    grid_dep_launch();
 
     const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
     const int m_tiles = p.m_tiles_dev ? *p.m_tiles_dev : p.m_tiles_host;  // 256-row tiles
@@ -287,36 +289,26 @@ cudaError_t gemm2_prepare(int fmt) {
 
 template <int FMT, bool L1>
 static cudaError_t launch2_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                             cudaStream_t st) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Gemm2Cfg<FMT>::SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+                             cudaStream_t st, bool pdl) {
+    LaunchAttrs at(pdl, 2);
+    cudaLaunchConfig_t cfg = at.config(dim3(grid), dim3(GEMM_THREADS), Gemm2Cfg<FMT>::SMEM, st);
     return cudaLaunchKernelEx(&cfg, grouped_gemm2_kernel<FMT, L1>, tmA, tmB, a);
 }
 
 // grid: an even number of CTAs (pairs); the B tensor map's box is 128 rows (one half)
 cudaError_t launch_gemm2(int fmt, bool l1, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                         int grid, cudaStream_t st) {
+                         int grid, cudaStream_t st, bool pdl) {
     if (grid % 2) return cudaErrorInvalidValue;
     switch (fmt) {
         case MOE_FMT_BF16:
-            return l1 ? launch2_t<MOE_FMT_BF16, true>(tmA, tmB, a, grid, st)
-                      : launch2_t<MOE_FMT_BF16, false>(tmA, tmB, a, grid, st);
+            return l1 ? launch2_t<MOE_FMT_BF16, true>(tmA, tmB, a, grid, st, pdl)
+                      : launch2_t<MOE_FMT_BF16, false>(tmA, tmB, a, grid, st, pdl);
         case MOE_FMT_MXFP8:
-            return l1 ? launch2_t<MOE_FMT_MXFP8, true>(tmA, tmB, a, grid, st)
-                      : launch2_t<MOE_FMT_MXFP8, false>(tmA, tmB, a, grid, st);
+            return l1 ? launch2_t<MOE_FMT_MXFP8, true>(tmA, tmB, a, grid, st, pdl)
+                      : launch2_t<MOE_FMT_MXFP8, false>(tmA, tmB, a, grid, st, pdl);
         default:
-            return l1 ? launch2_t<MOE_FMT_NVFP4, true>(tmA, tmB, a, grid, st)
-                      : launch2_t<MOE_FMT_NVFP4, false>(tmA, tmB, a, grid, st);
+            return l1 ? launch2_t<MOE_FMT_NVFP4, true>(tmA, tmB, a, grid, st, pdl)
+                      : launch2_t<MOE_FMT_NVFP4, false>(tmA, tmB, a, grid, st, pdl);
     }
 }
 

@@ -8,6 +8,37 @@
 
 namespace moe {
 
+// Launch attributes: programmatic stream serialisation (pdl) and an optional cluster
+// size. The attribute array must outlive the launch call only.
+struct LaunchAttrs {
+    cudaLaunchAttribute a[2];
+    int n = 0;
+    LaunchAttrs(bool pdl, int cluster = 1) {
+        if (pdl) {
+            a[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            a[n].val.programmaticStreamSerializationAllowed = 1;
+            ++n;
+        }
+        if (cluster > 1) {
+            a[n].id = cudaLaunchAttributeClusterDimension;
+            a[n].val.clusterDim.x = (unsigned)cluster;
+            a[n].val.clusterDim.y = 1;
+            a[n].val.clusterDim.z = 1;
+            ++n;
+        }
+    }
+    cudaLaunchConfig_t config(dim3 grid, dim3 block, size_t smem, cudaStream_t st) {
+        cudaLaunchConfig_t c = {};
+        c.gridDim = grid;
+        c.blockDim = block;
+        c.dynamicSmemBytes = smem;
+        c.stream = st;
+        c.attrs = a;
+        c.numAttrs = (unsigned)n;
+        return c;
+    }
+};
+
 // ------------------------------------------------------------------ routing
 // Histogram, BLOCK_M (bm)-padded offsets, stable scatter (one CTA). Writes cnt[E],
 // off[E+1], src[M_pad] (-1 padding), inv[T*k] (-1 masked), tile_expert[M_pad/bm],
@@ -15,7 +46,7 @@ namespace moe {
 size_t route_smem_bytes(int E);
 cudaError_t route_prepare(int E);   // sets the dynamic shared memory attribute (E <= 512)
 cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int bm, int* cnt, int* off, int* src, int* inv,
-                         int* tile_expert, int* meta, int* err, cudaStream_t st);
+                         int* tile_expert, int* meta, int* err, cudaStream_t st, bool pdl = false);
 
 // ------------------------------------------------------------------ dispatch quantisation
 struct DispatchArgs {
@@ -30,7 +61,7 @@ struct DispatchArgs {
     uint8_t* sxq;        // [T_pad, H/vpe] identity rows
     uint8_t* sxsf;
 };
-cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st);
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl = false);
 
 // ------------------------------------------------------------------ grouped GEMM
 struct GemmArgs {
@@ -67,10 +98,10 @@ cudaError_t gemm_prepare(int fmt);   // sets the dynamic shared memory attribute
 // CTA-pair variant: 256 x 256 tiles over 256-row segments; the B map's box is 128 rows
 cudaError_t gemm2_prepare(int fmt);
 cudaError_t launch_gemm2(int fmt, bool l1, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                         int grid, cudaStream_t st);
+                         int grid, cudaStream_t st, bool pdl = false);
 // bn: 128 or 256 (the tile width; the B tensor map's box must be bn rows)
 cudaError_t launch_gemm(int fmt, bool l1, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                        int grid, cudaStream_t st);
+                        int grid, cudaStream_t st, bool pdl = false);
 
 // ------------------------------------------------------------------ combine
 struct CombineArgs {
@@ -84,7 +115,7 @@ struct CombineArgs {
     __nv_bfloat16* out;        // [T, H]
 };
 cudaError_t combine_prepare();   // allows the norm's [H] fp32 shared-memory row (H <= 16384)
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl = false);
 
 // ------------------------------------------------------------------ weight transform
 cudaError_t launch_interleave_rows(const uint8_t* src, uint8_t* dst, int E, int I, int64_t row_bytes,

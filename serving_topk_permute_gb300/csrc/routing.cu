@@ -40,6 +40,9 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     const int beg = min(warp * chunk, R), end = min(beg + chunk, R);
 
     for (int i = tid; i < ROUTE_WARPS * E; i += ROUTE_THREADS) wcnt[i] = 0;
+    grid_dep_wait();  // the previous kernel (which may still read src / inv) has finished
+    grid_dep_launch();
+    if (tid == 0 && err) *err = 0;  // the status word reflects this forward only
     __syncthreads();
 
     // pass 1: per-warp histograms (ids loaded RB groups of 32 at a time: independent loads in flight)
@@ -152,10 +155,10 @@ cudaError_t route_prepare(int E) {
 }
 
 cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int bm, int* cnt, int* off, int* src, int* inv,
-                         int* tile_expert, int* meta, int* err, cudaStream_t st) {
-    const size_t smem = route_smem_bytes(E);
-    route_kernel<<<1, ROUTE_THREADS, smem, st>>>(ids, T, k, E, bm, cnt, off, src, inv, tile_expert, meta, err);
-    return cudaGetLastError();
+                         int* tile_expert, int* meta, int* err, cudaStream_t st, bool pdl) {
+    LaunchAttrs at(pdl);
+    cudaLaunchConfig_t cfg = at.config(dim3(1), dim3(ROUTE_THREADS), route_smem_bytes(E), st);
+    return cudaLaunchKernelEx(&cfg, route_kernel, ids, T, k, E, bm, cnt, off, src, inv, tile_expert, meta, err);
 }
 
 }  // namespace moe

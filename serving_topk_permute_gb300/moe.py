@@ -26,6 +26,7 @@ REGIONS = {"counts": 0, "offsets": 1, "src": 2, "inv_perm": 3, "xq": 4, "xsf": 5
 FLAG_DEBUG_H = 1
 FLAG_TILE = {0: 0, 128: 2, 256: 4}   # GEMM tile width: 0 = the library's choice
 FLAG_CTA = {"auto": 0, "pair": 8, "single": 16}   # GEMMs on CTA pairs: by rows per expert / always / never
+FLAG_SERIAL = 32   # no programmatic dependent launch between the forward's kernels
 KERNELS = ["route", "dispatch", "l1", "l2", "shared_l1", "shared_l2", "combine"]
 
 
@@ -147,13 +148,15 @@ class LayerConfig:
     debug_h: bool = False
     tile: int = 0
     cta: str = "auto"
+    serial: bool = False
 
     def to_c(self) -> Config:
         return Config(self.num_experts, self.hidden, self.inter, self.top_k, self.max_tokens, FORMATS[self.fmt], 0,
                       self.act_alpha, self.act_beta, 0.0 if self.act_clamp is None else self.act_clamp,
                       0 if self.act_clamp is None else 1, self.shared_inter, FORMATS[self.shared_fmt],
                       1 if self.post_norm else 0, self.norm_eps,
-                      (FLAG_DEBUG_H if self.debug_h else 0) | FLAG_TILE[self.tile] | FLAG_CTA[self.cta])
+                      (FLAG_DEBUG_H if self.debug_h else 0) | FLAG_TILE[self.tile] | FLAG_CTA[self.cta]
+                      | (FLAG_SERIAL if self.serial else 0))
 
 
 def validate(cfg: LayerConfig) -> int:
