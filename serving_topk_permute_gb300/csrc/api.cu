@@ -171,6 +171,17 @@ bool map_3d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t N, ui
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// an array of 512-byte scale atoms as a 2-D uint32 tensor [atoms][128], loaded box_atoms at a time
+bool map_atoms(CUtensorMap* m, const void* base, uint64_t atoms, uint32_t box_atoms) {
+    cuuint64_t dims[2] = {ATOM_BYTES / 4, atoms};
+    cuuint64_t strides[1] = {ATOM_BYTES};
+    cuuint32_t box[2] = {ATOM_BYTES / 4, box_atoms};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 
 }  // namespace
@@ -397,8 +408,9 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool p
                    uint8_t* hq, uint8_t* hsf, float* h_debug, __nv_bfloat16* y, int* err, bool activation,
                    cudaStream_t st) {
     const moe_config_t& c = p->cfg;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tsa, tsb;
     GemmArgs g{};
+    const int S = fmt_sf_atoms(fmt);
     g.m_tiles_dev = m_tiles_dev;
     g.m_tiles_host = m_tiles_host;
     g.tile_expert = tile_expert;
@@ -416,7 +428,7 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool p
     auto launch = [&](bool l1, int64_t tiles) {
         if (pair) {
             const int grid = 2 * (int)std::min<int64_t>(p->num_sms / 2, std::max<int64_t>(1, tiles));
-            return launch_gemm2(fmt, l1, ta, tb, g, grid, st, p->pdl);
+            return launch_gemm2(fmt, l1, ta, tb, S ? tsa : ta, S ? tsb : tb, g, grid, st, p->pdl);
         }
         const int grid = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, tiles));
         return launch_gemm(fmt, l1, bn, ta, tb, g, grid, st, p->pdl);
@@ -429,6 +441,11 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool p
     g.nks = (int)fmt_k_stages(fmt, H);
     g.n_tiles = (int)ceil_div(2 * I, bn);
     g.sf_blocks = (int)wt_sf_blocks(2 * I);
+    if (pair && S) {
+        if (!map_atoms(&tsa, xsf, (uint64_t)(rows / BM) * g.nks * S, S)) return MOE_ERR_CUDA;
+        if (!map_atoms(&tsb, w->w13_sf, (uint64_t)E * g.nks * g.sf_blocks * S, S * (2 * BM / NBLK)))
+            return MOE_ERR_CUDA;
+    }
     g.N = 2 * I;
     g.x_scale = x_scale;
     g.gscale = w->w13_gs;
@@ -450,6 +467,11 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool p
     g.nks = (int)fmt_k_stages(fmt, I);
     g.n_tiles = (int)ceil_div(H, bn);
     g.sf_blocks = (int)wt_sf_blocks(H);
+    if (pair && S) {
+        if (!map_atoms(&tsa, hsf, (uint64_t)(rows / BM) * g.nks * S, S)) return MOE_ERR_CUDA;
+        if (!map_atoms(&tsb, w->w2_sf, (uint64_t)E * g.nks * g.sf_blocks * S, S * (2 * BM / NBLK)))
+            return MOE_ERR_CUDA;
+    }
     g.N = H;
     g.gscale = w->w2_gs;
     g.y = y;

@@ -6,13 +6,16 @@
 // its own 128 A rows and one half (128 rows) of the 256 weight rows per K stage
 // (32 KB instead of 48 KB, so 5-6 stages fit instead of 4), plus the scale atoms
 // its tensor-memory copy needs (its A rows' atoms and both weight halves' atoms).
-// The leader CTA's MMA thread issues 256x256xK MMAs that read both CTAs' shared
-// memory and write each CTA's 128 accumulator rows into its own tensor memory,
-// and commits to the barriers of both CTAs at once. The follower's warp 1
-// forwards "stage landed" from its local barrier to the leader's; the follower's
-// epilogue warps report "accumulator read" to the leader the same way. Tiles are
-// walked row-tile-major and strided over the clusters. Every pipeline wait is
-// bounded; a CTA that gives up still waits for its own copies and MMAs.
+// Both CTAs' loads are cta_group::2 tensor copies that complete on the leader's
+// "full" barrier, on which each producer arrives with its own byte count (the
+// follower remotely); so the leader's MMA thread starts a stage as soon as both
+// halves have landed. It issues 256x256xK MMAs that read both CTAs' shared memory
+// and write each CTA's 128 accumulator rows into its own tensor memory, and
+// commits to the barriers of both CTAs at once. The follower's epilogue warps
+// report "accumulator read" to the leader. Tiles are walked row-tile-major and
+// strided over the clusters. Every pipeline wait is bounded; at the end the
+// producers exchange how many stages each issued, so that every issued copy
+// lands before either CTA exits, also when one of them gave up.
 #include "gemm_epilogue.cuh"
 
 namespace moe {
@@ -40,16 +43,18 @@ struct Gemm2Cfg {
 template <int FMT, bool L1>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     grouped_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                          const GemmArgs p) {
     using C = Gemm2Cfg<FMT>;
     constexpr int S = C::S, NB = C::NB, STAGES = C::STAGES, BN = C::BN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
-    // barriers: full[STAGES], empty[STAGES], tfull, tempty, drain
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3);
+    // barriers: full[STAGES], empty[STAGES], tfull, tempty, drain, teardown
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* never = reinterpret_cast<int*>(tmem_slot + 2);
+    volatile uint32_t* peer_issued = tmem_slot + 3;  // leader: stages the follower's producer issued
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_ctarank();
@@ -58,21 +63,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t tfull_bar = bar0 + 8 * (2 * STAGES);
     const uint32_t tempty_bar = tfull_bar + 8;
     const uint32_t drain_bar = tfull_bar + 16;
+    const uint32_t teardown_bar = tfull_bar + 24;
     const uint64_t tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar0 + 8 * s, leader ? 2 : 1);     // full: own loads (+ the follower's forward)
+            mbar_init(bar0 + 8 * s, leader ? 2 : 1);     // full (the leader's counts): both producers arrive
             mbar_init(bar0 + 8 * (STAGES + s), 1);       // empty: the leader's commit
         }
         mbar_init(tfull_bar, 1);
         mbar_init(tempty_bar, leader ? 2 * EPI_WARPS : EPI_WARPS);
         mbar_init(drain_bar, 1);
+        mbar_init(teardown_bar, 1);
         *abort_flag = 0;
+        *peer_issued = 0;
         *never = 0;
         fence_mbar_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        if constexpr (C::S > 0) {
+            prefetch_tmap(&tmSFA);
+            prefetch_tmap(&tmSFB);
+        }
     }
     if (warp == 1) {
         tmem_alloc2(smem_u32(tmem_slot), TMEM_COLS);
@@ -97,45 +109,65 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {
+            // Both CTAs count their bytes on the leader's full barrier: each arrives on it
+            // with its own transaction count (the follower remotely), and its loads
+            // complete on it (cta_group::2), so the leader's MMA thread sees a stage
+            // as soon as both halves have landed.
+            const uint32_t full_cl0 = mapa_shared(bar0, 0);
             int stage = 0;
             uint32_t phase = 0;
-            int last_parity[STAGES];
-#pragma unroll
-            for (int s = 0; s < STAGES; ++s) last_parity[s] = -1;
+            uint32_t issued = 0;
             bool ok = true;
             for (int tile = pair; ok && tile < total; tile += npairs) {
                 const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
                 const int e = p.tile_expert ? p.tile_expert[mt] : 0;
                 const int a_tile = 2 * mt + (int)rank;  // this CTA's 128-row tile
                 for (int ks = 0; ks < p.nks; ++ks) {
-                    const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (STAGES + stage);
+                    const uint32_t empty = bar0 + 8 * (STAGES + stage), full_cl = full_cl0 + 8 * stage;
                     if (!mbar_wait(empty, phase ^ 1, tmo, abort_flag)) {
                         give_up();
                         ok = false;
                         break;
                     }
                     const uint32_t st = smem_u32(smem + stage * C::STAGE_BYTES);
-                    mbar_arrive_expect_tx(full, C::TX_BYTES);
-                    tma_load_2d(st, &tmA, full, ks * BK_BYTES, a_tile * BM);
-                    tma_load_3d(st + C::A_BYTES, &tmB, full, ks * BK_BYTES, nt * BN + (int)rank * NBLK, e);
+                    if (leader)
+                        mbar_arrive_expect_tx(bar0 + 8 * stage, C::TX_BYTES);
+                    else
+                        mbar_arrive_expect_tx_cluster(full_cl, C::TX_BYTES);
+                    tma_load_2d_cg2(st, &tmA, full_cl, ks * BK_BYTES, a_tile * BM);
+                    tma_load_3d_cg2(st + C::A_BYTES, &tmB, full_cl, ks * BK_BYTES, nt * BN + (int)rank * NBLK, e);
                     if constexpr (S > 0) {
-                        bulk_load(st + C::A_BYTES + C::B_BYTES,
-                                  p.sfa + ((int64_t)a_tile * p.nks + ks) * C::SFA_BYTES, C::SFA_BYTES, full);
-                        const int64_t blk = ((int64_t)e * p.nks + ks) * p.sf_blocks + (int64_t)nt * NB;
-                        bulk_load(st + C::A_BYTES + C::B_BYTES + C::SFA_BYTES, p.sfb + blk * S * ATOM_BYTES,
-                                  C::SFB_BYTES, full);
+                        tma_load_2d_cg2(st + C::A_BYTES + C::B_BYTES, &tmSFA, full_cl, 0,
+                                        (a_tile * p.nks + ks) * S);
+                        tma_load_2d_cg2(st + C::A_BYTES + C::B_BYTES + C::SFA_BYTES, &tmSFB, full_cl, 0,
+                                        ((e * p.nks + ks) * p.sf_blocks + nt * NB) * S);
                     }
-                    last_parity[stage] = (int)phase;
+                    ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
-            // every load this CTA issued lands before it may exit (the leader's full barrier
-            // also needs the follower's forward, so a leader that gave up may wait the limit)
-            for (int s = 0; s < STAGES; ++s)
-                if (last_parity[s] >= 0) mbar_wait(bar0 + 8 * s, (uint32_t)last_parity[s], DRAIN_TIMEOUT_NS, never);
+            // Every load either CTA issued lands before the pair may exit. The follower
+            // reports its count to the leader; for a stage only one CTA issued (one of
+            // them gave up), the leader supplies the missing arrival, so that the stage's
+            // phase completes once the issued bytes have landed. A producer can run at
+            // most STAGES stages ahead of the other one (a slot is reused only after the
+            // MMA consumed it, which needs both arrivals), so each slot is touched once.
+            if (!leader) {
+                st_cluster_u32(mapa_shared(smem_u32((const void*)peer_issued), 0), issued);
+                mbar_arrive_release_cluster(mapa_shared(teardown_bar, 0));
+            } else {
+                uint32_t other = issued;
+                if (mbar_wait_cl(teardown_bar, 0, DRAIN_TIMEOUT_NS, never)) other = *peer_issued;
+                const uint32_t lo = min(issued, other), hi = max(issued, other);
+                for (uint32_t n = lo; n < hi; ++n) mbar_arrive(bar0 + 8 * (n % STAGES));
+                for (uint32_t s = 0; s < (uint32_t)STAGES && s < hi; ++s) {
+                    const uint32_t last = s + (hi - 1 - s) / STAGES * STAGES;  // last stage n < hi in slot s
+                    mbar_wait(bar0 + 8 * s, (last / STAGES) & 1u, DRAIN_TIMEOUT_NS, never);
+                }
+            }
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
@@ -203,26 +235,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 tc_commit2_mc(drain_bar, 0x1);
                 mbar_wait(drain_bar, 0, DRAIN_TIMEOUT_NS, never);
             }
-        } else if (lane == 0) {
-            // follower: forward "stage landed" to the leader's full barrier, in stage order
-            const uint32_t leader_full0 = mapa_shared(bar0, 0);
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int tile = pair; ok && tile < total; tile += npairs) {
-                for (int ks = 0; ks < p.nks; ++ks) {
-                    if (!mbar_wait(bar0 + 8 * stage, phase, tmo, abort_flag)) {
-                        give_up();
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_cluster(leader_full0 + 8 * stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-            }
         }
     } else {
         const int q = warp % 4;
@@ -288,27 +300,27 @@ cudaError_t gemm2_prepare(int fmt) {
 }
 
 template <int FMT, bool L1>
-static cudaError_t launch2_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                             cudaStream_t st, bool pdl) {
+static cudaError_t launch2_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
+                             const CUtensorMap& tmSFB, const GemmArgs& a, int grid, cudaStream_t st, bool pdl) {
     LaunchAttrs at(pdl, 2);
     cudaLaunchConfig_t cfg = at.config(dim3(grid), dim3(GEMM_THREADS), Gemm2Cfg<FMT>::SMEM, st);
-    return cudaLaunchKernelEx(&cfg, grouped_gemm2_kernel<FMT, L1>, tmA, tmB, a);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm2_kernel<FMT, L1>, tmA, tmB, tmSFA, tmSFB, a);
 }
 
 // grid: an even number of CTAs (pairs); the B tensor map's box is 128 rows (one half)
-cudaError_t launch_gemm2(int fmt, bool l1, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                         int grid, cudaStream_t st, bool pdl) {
+cudaError_t launch_gemm2(int fmt, bool l1, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
+                         const CUtensorMap& tmSFB, const GemmArgs& a, int grid, cudaStream_t st, bool pdl) {
     if (grid % 2) return cudaErrorInvalidValue;
     switch (fmt) {
         case MOE_FMT_BF16:
-            return l1 ? launch2_t<MOE_FMT_BF16, true>(tmA, tmB, a, grid, st, pdl)
-                      : launch2_t<MOE_FMT_BF16, false>(tmA, tmB, a, grid, st, pdl);
+            return l1 ? launch2_t<MOE_FMT_BF16, true>(tmA, tmB, tmSFA, tmSFB, a, grid, st, pdl)
+                      : launch2_t<MOE_FMT_BF16, false>(tmA, tmB, tmSFA, tmSFB, a, grid, st, pdl);
         case MOE_FMT_MXFP8:
-            return l1 ? launch2_t<MOE_FMT_MXFP8, true>(tmA, tmB, a, grid, st, pdl)
-                      : launch2_t<MOE_FMT_MXFP8, false>(tmA, tmB, a, grid, st, pdl);
+            return l1 ? launch2_t<MOE_FMT_MXFP8, true>(tmA, tmB, tmSFA, tmSFB, a, grid, st, pdl)
+                      : launch2_t<MOE_FMT_MXFP8, false>(tmA, tmB, tmSFA, tmSFB, a, grid, st, pdl);
         default:
-            return l1 ? launch2_t<MOE_FMT_NVFP4, true>(tmA, tmB, a, grid, st, pdl)
-                      : launch2_t<MOE_FMT_NVFP4, false>(tmA, tmB, a, grid, st, pdl);
+            return l1 ? launch2_t<MOE_FMT_NVFP4, true>(tmA, tmB, tmSFA, tmSFB, a, grid, st, pdl)
+                      : launch2_t<MOE_FMT_NVFP4, false>(tmA, tmB, tmSFA, tmSFB, a, grid, st, pdl);
     }
 }
 

@@ -97,8 +97,10 @@ struct GemmArgs {
 cudaError_t gemm_prepare(int fmt);   // sets the dynamic shared memory attribute of every variant
 // CTA-pair variant: 256 x 256 tiles over 256-row segments; the B map's box is 128 rows
 cudaError_t gemm2_prepare(int fmt);
-cudaError_t launch_gemm2(int fmt, bool l1, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                         int grid, cudaStream_t st, bool pdl = false);
+// tmSFA / tmSFB: the scale atoms as 2-D uint32 tensors [atoms][128] with boxes of
+// S (activation) and S * 2 (weight) atoms; unused for BF16
+cudaError_t launch_gemm2(int fmt, bool l1, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
+                         const CUtensorMap& tmSFB, const GemmArgs& a, int grid, cudaStream_t st, bool pdl = false);
 // bn: 128 or 256 (the tile width; the B tensor map's box must be bn rows)
 cudaError_t launch_gemm(int fmt, bool l1, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                         int grid, cudaStream_t st, bool pdl = false);
