@@ -431,7 +431,9 @@ def run_ours(args, shape: S.MoeShape):
     avg_k = {k_: statistics.mean(v) for k_, v in ktimes.items() if v and max(v) > 0}
     dominant = max(avg_k, key=avg_k.get)
     peaks, source = load_peaks()
-    rl = roofline(dominant, work, avg_k[dominant], peaks, source, sustained=False)
+    # the sustained (power-capped) tensor peak when the power cap acted during the timed steps, else the burst one
+    rl = roofline(dominant, work, avg_k[dominant], peaks, source,
+                  sustained="sw_power_cap" in (clk.get("reasons") or []))
     if (shape.name, dominant) in NCU_TRAFFIC:
         rl["traffic"], rl["traffic_source"] = NCU_TRAFFIC[(shape.name, dominant)]
     rl["kernel_ms"] = {k_: round(v, 4) for k_, v in avg_k.items()}
