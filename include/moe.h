@@ -60,6 +60,9 @@ extern "C" {
 #define MOE_FLAG_TILE_256 4u       /* 256-wide GEMM tiles (the default) */
 #define MOE_FLAG_CTA_PAIR 8u       /* run the GEMMs on CTA pairs (256 x 256 tiles, BLOCK_M 256) */
 #define MOE_FLAG_CTA_SINGLE 16u    /* run the GEMMs on single CTAs (the default) */
+#define MOE_FLAG_SPLIT_GEMM 64u    /* run L1 and L2 as two kernels (by default, with 256-wide single-CTA tiles,
+                                      one persistent kernel takes all L1 tiles, then all L2 tiles, from one
+                                      counter, each L2 tile starting once its rows' L1 tiles are done) */
 #define MOE_FLAG_SERIAL   32u      /* launch each kernel only after the previous one has finished (by default
                                       a kernel's set-up overlaps the previous kernel's tail: programmatic
                                       dependent launch, with every read of the previous output after the wait) */

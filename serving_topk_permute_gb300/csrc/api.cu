@@ -79,7 +79,7 @@ int block_m_for(const moe_config_t& c, int T) { return use_pair(c, routed_rows_p
 // ------------------------------------------------------------------ workspace layout
 enum Region {
     R_ERR, R_META, R_CNT, R_OFF, R_TILE_EXPERT, R_SRC, R_INV, R_XSCALE, R_XQ, R_XSF, R_HQ, R_HSF, R_Y, R_HDBG,
-    R_SXQ, R_SXSF, R_SHQ, R_SHSF, R_SY, R_COUNT
+    R_SXQ, R_SXSF, R_SHQ, R_SHSF, R_SY, R_SCHED, R_COUNT
 };
 
 struct Layout {
@@ -123,6 +123,9 @@ Layout layout_of(const moe_config_t& c, int T) {
         sz[R_SHSF] = (L.t_pad / BM) * fmt_k_stages(d.sfmt, d.Is) * Ss * ATOM_BYTES;
         sz[R_SY] = L.t_pad * d.H * 2;
     }
+    // schedule counters of the one-kernel GEMM: routed (counter, done[m_tiles_max]),
+    // then shared (counter, done[t_pad / 128]); zeroed by the routing kernel
+    sz[R_SCHED] = 4 * (2 + L.m_tiles_max + L.t_pad / BM);
     int64_t o = 0;
     for (int r = 0; r < R_COUNT; ++r) {
         L.off[r] = o;
@@ -244,6 +247,7 @@ int moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     for (int f = MOE_FMT_BF16; f <= MOE_FMT_NVFP4; ++f) {
         CUDA_TRY(gemm_prepare(f));
         CUDA_TRY(gemm2_prepare(f));
+        CUDA_TRY(fused_prepare(f));
     }
     CUDA_TRY(combine_prepare());
     moe_plan_s* p = new (std::nothrow) moe_plan_s;
@@ -400,17 +404,22 @@ static int choose_bn(const moe_config_t& c, int64_t rows_per_expert) {
     return 256;
 }
 
-// one expert MLP pass; m_tiles_* count 128-row tiles on single CTAs, 256-row tiles on pairs
+// one expert MLP pass; m_tiles_* count 128-row tiles on single CTAs, 256-row tiles on pairs.
+// With 256-wide single-CTA tiles (the default), L1 and L2 run as one kernel (sched:
+// its zeroed counters); otherwise as two.
 static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool pair, const void* xq,
                    const uint8_t* xsf, int64_t rows,
                    const moe_weights_t* w, const int* m_tiles_dev, int m_tiles_host, int64_t m_tiles_max,
                    const int* tile_expert, const int* src, int m_valid, const float* x_scale, const float* a2,
                    uint8_t* hq, uint8_t* hsf, float* h_debug, __nv_bfloat16* y, int* err, bool activation,
-                   cudaStream_t st) {
+                   uint32_t* sched, cudaStream_t st) {
     const moe_config_t& c = p->cfg;
-    CUtensorMap ta, tb, tsa, tsb;
-    GemmArgs g{};
     const int S = fmt_sf_atoms(fmt);
+    const int bn = pair ? 2 * BM : choose_bn(c, 0);
+    const uint32_t b_box = pair ? NBLK : bn;  // a CTA of a pair loads half of the 256 weight rows
+    const bool fused = !pair && bn == 256 && sched && !(c.flags & MOE_FLAG_SPLIT_GEMM);
+    CUtensorMap ta1, tb1, ta2, tb2, tsa1, tsb1, tsa2, tsb2;
+    GemmArgs g{};
     g.m_tiles_dev = m_tiles_dev;
     g.m_tiles_host = m_tiles_host;
     g.tile_expert = tile_expert;
@@ -423,62 +432,71 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool p
     g.act_beta = activation ? c.act_beta : 0.0f;
     g.act_clamp = c.act_clamp;
     g.act_has_clamp = activation ? c.act_has_clamp : 0;
-    const int bn = pair ? 2 * BM : choose_bn(c, 0);
-    const uint32_t b_box = pair ? NBLK : bn;  // a CTA of a pair loads half of the 256 weight rows
-    auto launch = [&](bool l1, int64_t tiles) {
-        if (pair) {
-            const int grid = 2 * (int)std::min<int64_t>(p->num_sms / 2, std::max<int64_t>(1, tiles));
-            return launch_gemm2(fmt, l1, ta, tb, S ? tsa : ta, S ? tsb : tb, g, grid, st, p->pdl);
-        }
-        const int grid = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, tiles));
-        return launch_gemm(fmt, l1, bn, ta, tb, g, grid, st, p->pdl);
-    };
-    // L1: [rows, H] x w13[e]^T -> h [rows, I]
-    if (!map_2d(&ta, xq, fmt_row_bytes(fmt, H), rows, BM)) return MOE_ERR_CUDA;
-    if (!map_3d(&tb, w->w13, fmt_row_bytes(fmt, H), 2 * (uint64_t)I, E, b_box)) return MOE_ERR_CUDA;
-    g.sfa = xsf;
-    g.sfb = (const uint8_t*)w->w13_sf;
-    g.nks = (int)fmt_k_stages(fmt, H);
-    g.n_tiles = (int)ceil_div(2 * I, bn);
-    g.sf_blocks = (int)wt_sf_blocks(2 * I);
-    if (pair && S) {
-        if (!map_atoms(&tsa, xsf, (uint64_t)(rows / BM) * g.nks * S, S)) return MOE_ERR_CUDA;
-        if (!map_atoms(&tsb, w->w13_sf, (uint64_t)E * g.nks * g.sf_blocks * S, S * (2 * BM / NBLK)))
-            return MOE_ERR_CUDA;
-    }
-    g.N = 2 * I;
     g.x_scale = x_scale;
-    g.gscale = w->w13_gs;
     g.a2 = a2;
     g.hq = hq;
     g.hsf = hsf;
     g.I = I;
     g.h_nks = (int)fmt_k_stages(fmt, I);
     g.h_debug = h_debug;
-    {
-        KernelTimer kt(p, kid1, st);
-        CUDA_TRY(launch(true, m_tiles_max * g.n_tiles));
-    }
-    // L2: h [rows, I] x w2[e]^T -> y [rows, H]
-    if (!map_2d(&ta, hq, fmt_row_bytes(fmt, I), rows, BM)) return MOE_ERR_CUDA;
-    if (!map_3d(&tb, w->w2, fmt_row_bytes(fmt, I), H, E, b_box)) return MOE_ERR_CUDA;
-    g.sfa = hsf;
-    g.sfb = (const uint8_t*)w->w2_sf;
-    g.nks = (int)fmt_k_stages(fmt, I);
-    g.n_tiles = (int)ceil_div(H, bn);
-    g.sf_blocks = (int)wt_sf_blocks(H);
-    if (pair && S) {
-        if (!map_atoms(&tsa, hsf, (uint64_t)(rows / BM) * g.nks * S, S)) return MOE_ERR_CUDA;
-        if (!map_atoms(&tsb, w->w2_sf, (uint64_t)E * g.nks * g.sf_blocks * S, S * (2 * BM / NBLK)))
-            return MOE_ERR_CUDA;
-    }
-    g.N = H;
-    g.gscale = w->w2_gs;
     g.y = y;
     g.ldy = H;
+    // L1: [rows, H] x w13[e]^T -> h [rows, I]
+    GemmArgs g1 = g;
+    g1.sfa = xsf;
+    g1.sfb = (const uint8_t*)w->w13_sf;
+    g1.nks = (int)fmt_k_stages(fmt, H);
+    g1.n_tiles = (int)ceil_div(2 * I, bn);
+    g1.sf_blocks = (int)wt_sf_blocks(2 * I);
+    g1.N = 2 * I;
+    g1.gscale = w->w13_gs;
+    if (!map_2d(&ta1, xq, fmt_row_bytes(fmt, H), rows, BM)) return MOE_ERR_CUDA;
+    if (!map_3d(&tb1, w->w13, fmt_row_bytes(fmt, H), 2 * (uint64_t)I, E, b_box)) return MOE_ERR_CUDA;
+    // L2: h [rows, I] x w2[e]^T -> y [rows, H]
+    GemmArgs g2 = g;
+    g2.sfa = hsf;
+    g2.sfb = (const uint8_t*)w->w2_sf;
+    g2.nks = (int)fmt_k_stages(fmt, I);
+    g2.n_tiles = (int)ceil_div(H, bn);
+    g2.sf_blocks = (int)wt_sf_blocks(H);
+    g2.N = H;
+    g2.gscale = w->w2_gs;
+    if (!map_2d(&ta2, hq, fmt_row_bytes(fmt, I), rows, BM)) return MOE_ERR_CUDA;
+    if (!map_3d(&tb2, w->w2, fmt_row_bytes(fmt, I), H, E, b_box)) return MOE_ERR_CUDA;
+    if (pair && S) {
+        const uint32_t sfb_box = (uint32_t)S * (2 * BM / NBLK);
+        if (!map_atoms(&tsa1, xsf, (uint64_t)(rows / BM) * g1.nks * S, S)) return MOE_ERR_CUDA;
+        if (!map_atoms(&tsb1, w->w13_sf, (uint64_t)E * g1.nks * g1.sf_blocks * S, sfb_box)) return MOE_ERR_CUDA;
+        if (!map_atoms(&tsa2, hsf, (uint64_t)(rows / BM) * g2.nks * S, S)) return MOE_ERR_CUDA;
+        if (!map_atoms(&tsb2, w->w2_sf, (uint64_t)E * g2.nks * g2.sf_blocks * S, sfb_box)) return MOE_ERR_CUDA;
+    }
+    if (fused) {
+        FusedSched fs{sched, sched + 1};
+        const int64_t tiles = m_tiles_max * (g1.n_tiles + g2.n_tiles);
+        const int grid = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, tiles));
+        KernelTimer kt(p, kid1, st);
+        CUDA_TRY(launch_fused_mlp(fmt, ta1, tb1, ta2, tb2, g1, g2, fs, grid, st, p->pdl));
+        return MOE_OK;
+    }
+    auto launch = [&](bool l1, const GemmArgs& ga, int64_t tiles) {
+        const CUtensorMap& ta = l1 ? ta1 : ta2;
+        const CUtensorMap& tb = l1 ? tb1 : tb2;
+        if (pair) {
+            const int grid = 2 * (int)std::min<int64_t>(p->num_sms / 2, std::max<int64_t>(1, tiles));
+            const CUtensorMap& tsa = S ? (l1 ? tsa1 : tsa2) : ta;
+            const CUtensorMap& tsb = S ? (l1 ? tsb1 : tsb2) : tb;
+            return launch_gemm2(fmt, l1, ta, tb, tsa, tsb, ga, grid, st, p->pdl);
+        }
+        const int grid = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, tiles));
+        return launch_gemm(fmt, l1, bn, ta, tb, ga, grid, st, p->pdl);
+    };
+    {
+        KernelTimer kt(p, kid1, st);
+        CUDA_TRY(launch(true, g1, m_tiles_max * g1.n_tiles));
+    }
     {
         KernelTimer kt(p, kid1 + 1, st);
-        CUDA_TRY(launch(false, m_tiles_max * g.n_tiles));
+        CUDA_TRY(launch(false, g2, m_tiles_max * g2.n_tiles));
     }
     return MOE_OK;
 }
@@ -516,7 +534,8 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
     {
         KernelTimer kt(plan, MOE_KERNEL_ROUTE, st);
         CUDA_TRY(launch_route(topk_ids, T, d.k, d.E, bm, (int*)R(R_CNT), (int*)R(R_OFF), (int*)R(R_SRC), (int*)R(R_INV),
-                          (int*)R(R_TILE_EXPERT), meta, err, st, plan->pdl));
+                          (int*)R(R_TILE_EXPERT), meta, err, st, plan->pdl, (uint32_t*)R(R_SCHED),
+                          (int)(L.size[R_SCHED] / 4)));
     }
     DispatchArgs da{};
     da.x = (const uint16_t*)hidden;
@@ -540,14 +559,14 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
                      meta + 1, 0, L.m_pad_max / bm,
                      (const int*)R(R_TILE_EXPERT), (const int*)R(R_SRC), 0, (const float*)R(R_XSCALE), l2_act_scale,
                      R(R_HQ), R(R_HSF), (c.flags & MOE_FLAG_DEBUG_H) ? (float*)R(R_HDBG) : nullptr,
-                     (__nv_bfloat16*)R(R_Y), err, true, st);
+                     (__nv_bfloat16*)R(R_Y), err, true, (uint32_t*)R(R_SCHED), st);
     if (rc != MOE_OK) return rc;
     if (d.Is > 0) {
         const bool shared_pair = use_pair(c, T);
         const int tiles = (int)(L.t_pad / (shared_pair ? 2 * BM : BM));
         rc = run_mlp(plan, MOE_KERNEL_SHARED_L1, d.sfmt, 1, d.Is, d.H, shared_pair, R(R_SXQ), R(R_SXSF), L.t_pad, shared, nullptr, tiles, tiles, nullptr,
                      nullptr, T, nullptr, nullptr, R(R_SHQ), R(R_SHSF), nullptr, (__nv_bfloat16*)R(R_SY), err, false,
-                     st);
+                     (uint32_t*)R(R_SCHED) + 1 + L.m_tiles_max, st);
         if (rc != MOE_OK) return rc;
     }
     CombineArgs ca{};

@@ -85,6 +85,21 @@ __device__ inline void set_error(int* err, int code) {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// ------------------------------------------------------------------ cross-CTA flags in global memory
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// orders this thread's generic-proxy global accesses with its later (or earlier)
+// async-proxy ones (TMA): data written with st.global and read back by TMA
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -164,6 +179,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     for (uint64_t round = 0;; ++round) {
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity, hint)) return true;
+        if (*abort) return false;
+        if (round >= max_rounds || globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+// Wait until *flag >= target (read with acquire at GPU scope), giving up after
+// timeout_ns or as soon as *abort is set. Returns false on give-up.
+__device__ __forceinline__ bool flag_wait_geq(const uint32_t* flag, uint32_t target, uint64_t timeout_ns,
+                                              const volatile int* abort) {
+    if (ld_acquire_gpu(flag) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    const uint64_t max_rounds = 1 + timeout_ns / 64;  // bounds the wait even where the timer ticks coarsely
+    for (uint64_t round = 0;; ++round) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(flag) >= target) return true;
         if (*abort) return false;
         if (round >= max_rounds || globaltimer_ns() - t0 > timeout_ns) return false;
     }

@@ -218,7 +218,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, tmo, abort_flag)) {
+            // warp-uniform: every lane leaves together (a lane left behind would block in __syncwarp)
+            if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, acc_phase, tmo, abort_flag))) {
                 give_up();
                 break;
             }

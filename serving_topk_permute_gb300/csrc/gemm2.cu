@@ -242,7 +242,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t leader_tempty = mapa_shared(tempty_bar, 0);
         uint32_t acc_phase = 0;
         for (int tile = pair; tile < total; tile += npairs) {
-            if (!mbar_wait(tfull_bar, acc_phase, tmo, abort_flag)) {
+            // warp-uniform: every lane leaves together (a lane left behind would block in __syncwarp)
+            if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar, acc_phase, tmo, abort_flag))) {
                 give_up();
                 break;
             }

@@ -45,8 +45,10 @@ struct LaunchAttrs {
 // meta[0] = M_pad, meta[1] = M_pad / bm.
 size_t route_smem_bytes(int E);
 cudaError_t route_prepare(int E);   // sets the dynamic shared memory attribute (E <= 512)
+// zero[0..n_zero): words the routing kernel also zeroes (the GEMM schedule counters)
 cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int bm, int* cnt, int* off, int* src, int* inv,
-                         int* tile_expert, int* meta, int* err, cudaStream_t st, bool pdl = false);
+                         int* tile_expert, int* meta, int* err, cudaStream_t st, bool pdl = false,
+                         uint32_t* zero = nullptr, int n_zero = 0);
 
 // ------------------------------------------------------------------ dispatch quantisation
 struct DispatchArgs {
@@ -95,6 +97,18 @@ struct GemmArgs {
     unsigned long long timeout_ns;
 };
 cudaError_t gemm_prepare(int fmt);   // sets the dynamic shared memory attribute of every variant
+
+// Both GEMMs in one persistent kernel (256-wide tiles, single CTAs). counter: the
+// next tile to take; done[m_tiles]: published L1 epilogue warps per row tile. Both
+// must be zero at launch (the routing kernel zeroes them).
+struct FusedSched {
+    uint32_t* counter;
+    uint32_t* done;
+};
+cudaError_t fused_prepare(int fmt);
+cudaError_t launch_fused_mlp(int fmt, const CUtensorMap& a1, const CUtensorMap& b1, const CUtensorMap& a2,
+                             const CUtensorMap& b2, const GemmArgs& p1, const GemmArgs& p2, const FusedSched& fs,
+                             int grid, cudaStream_t st, bool pdl = false);
 // CTA-pair variant: 256 x 256 tiles over 256-row segments; the B map's box is 128 rows
 cudaError_t gemm2_prepare(int fmt);
 // tmSFA / tmSFB: the scale atoms as 2-D uint32 tensors [atoms][128] with boxes of

@@ -28,7 +28,7 @@ constexpr int RB = 8;  // 32-slot groups whose ids are loaded together
 __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     route_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int bm, int* __restrict__ cnt,
                  int* __restrict__ off, int* __restrict__ src, int* __restrict__ inv, int* __restrict__ tile_expert,
-                 int* __restrict__ meta, int* err) {
+                 int* __restrict__ meta, int* err, uint32_t* __restrict__ zero, int n_zero) {
     extern __shared__ int sm[];
     int* wcnt = sm;                          // [32][E]: per-warp counts, then per-warp running bases
     int* s_off = sm + ROUTE_WARPS * E;       // [E+1]
@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     grid_dep_wait();  // the previous kernel (which may still read src / inv) has finished
     grid_dep_launch();
     if (tid == 0 && err) *err = 0;  // the status word reflects this forward only
+    for (int i = tid; i < n_zero; i += ROUTE_THREADS) zero[i] = 0u;
     __syncthreads();
 
     // pass 1: per-warp histograms (ids loaded RB groups of 32 at a time: independent loads in flight)
@@ -155,10 +156,12 @@ cudaError_t route_prepare(int E) {
 }
 
 cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int bm, int* cnt, int* off, int* src, int* inv,
-                         int* tile_expert, int* meta, int* err, cudaStream_t st, bool pdl) {
+                         int* tile_expert, int* meta, int* err, cudaStream_t st, bool pdl, uint32_t* zero,
+                         int n_zero) {
     LaunchAttrs at(pdl);
     cudaLaunchConfig_t cfg = at.config(dim3(1), dim3(ROUTE_THREADS), route_smem_bytes(E), st);
-    return cudaLaunchKernelEx(&cfg, route_kernel, ids, T, k, E, bm, cnt, off, src, inv, tile_expert, meta, err);
+    return cudaLaunchKernelEx(&cfg, route_kernel, ids, T, k, E, bm, cnt, off, src, inv, tile_expert, meta, err, zero,
+                              n_zero);
 }
 
 }  // namespace moe

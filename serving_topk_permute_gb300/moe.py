@@ -27,6 +27,7 @@ FLAG_DEBUG_H = 1
 FLAG_TILE = {0: 0, 128: 2, 256: 4}   # GEMM tile width: 0 = the library's choice
 FLAG_CTA = {"auto": 0, "pair": 8, "single": 16}   # GEMMs on CTA pairs: by rows per expert / always / never
 FLAG_SERIAL = 32   # no programmatic dependent launch between the forward's kernels
+FLAG_SPLIT_GEMM = 64   # L1 and L2 as two kernels instead of one
 KERNELS = ["route", "dispatch", "l1", "l2", "shared_l1", "shared_l2", "combine"]
 
 
@@ -149,6 +150,7 @@ class LayerConfig:
     tile: int = 0
     cta: str = "auto"
     serial: bool = False
+    split_gemm: bool = False
 
     def to_c(self) -> Config:
         return Config(self.num_experts, self.hidden, self.inter, self.top_k, self.max_tokens, FORMATS[self.fmt], 0,
@@ -156,7 +158,7 @@ class LayerConfig:
                       0 if self.act_clamp is None else 1, self.shared_inter, FORMATS[self.shared_fmt],
                       1 if self.post_norm else 0, self.norm_eps,
                       (FLAG_DEBUG_H if self.debug_h else 0) | FLAG_TILE[self.tile] | FLAG_CTA[self.cta]
-                      | (FLAG_SERIAL if self.serial else 0))
+                      | (FLAG_SERIAL if self.serial else 0) | (FLAG_SPLIT_GEMM if self.split_gemm else 0))
 
 
 def validate(cfg: LayerConfig) -> int:

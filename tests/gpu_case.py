@@ -106,13 +106,13 @@ def _ckpt_dev(ew: OM.ExpertWeights, touched=None) -> dict:
     return out
 
 
-def layer_config(case: Case, debug_h=False, max_tokens=None, tile=0, cta="auto") -> pkg.LayerConfig:
+def layer_config(case: Case, debug_h=False, max_tokens=None, tile=0, cta="auto", split=False) -> pkg.LayerConfig:
     s = case.shape
     act = case.layer.act
     return pkg.LayerConfig(s.E, s.H, s.I, s.k, max_tokens or max(case.x.shape[0], 1), s.fmt,
                            act_alpha=act.alpha, act_beta=act.beta, act_clamp=act.clamp,
                            shared_inter=s.shared_I, shared_fmt=s.shared_fmt, post_norm=s.post_norm,
-                           norm_eps=s.norm_eps, debug_h=debug_h, tile=tile, cta=cta)
+                           norm_eps=s.norm_eps, debug_h=debug_h, tile=tile, cta=cta, split_gemm=split)
 
 
 @dataclass
@@ -125,13 +125,14 @@ class GpuRun:
     inputs: dict
 
 
-# GEMM variants: single CTA with 128- or 256-wide tiles, or CTA pairs (256 x 256 tiles)
-MODES = {"single128": dict(tile=128, cta="single"), "single256": dict(tile=256, cta="single"),
-         "pair": dict(cta="pair")}
+# GEMM variants: L1 and L2 in one kernel (256-wide single-CTA tiles, the default); two
+# single-CTA kernels with 128- or 256-wide tiles; CTA pairs (256 x 256 tiles, two kernels)
+MODES = {"fused": dict(tile=256, cta="single"), "single128": dict(tile=128, cta="single"),
+         "split256": dict(tile=256, cta="single", split=True), "pair": dict(cta="pair")}
 
 
-def run_gpu(case: Case, debug_h=False, max_tokens=None, tile=0, cta="auto") -> GpuRun:
-    plan = pkg.Plan(layer_config(case, debug_h, max_tokens, tile, cta))
+def run_gpu(case: Case, debug_h=False, max_tokens=None, tile=0, cta="auto", split=False) -> GpuRun:
+    plan = pkg.Plan(layer_config(case, debug_h, max_tokens, tile, cta, split))
     ck = _ckpt_dev(case.layer.routed, case.touched)
     kw = plan.transform_weights(ck)
     ks = None

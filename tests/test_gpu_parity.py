@@ -91,8 +91,9 @@ def test_routing_and_dispatch_bit_exact_full_size(name):
 @pytest.mark.parametrize("mode", list(G.MODES))
 @pytest.mark.parametrize("name", list(REDUCED))
 def test_forward_matches_oracle_reduced(name, mode):
-    """Every GEMM variant: single CTA with 128-wide tiles (double-buffered accumulators) or
-    256-wide tiles, and CTA pairs (256 x 256 tiles over 256-row segments)."""
+    """Every GEMM variant: L1 and L2 in one kernel (the default); two single-CTA kernels with
+    128-wide tiles (double-buffered accumulators) or 256-wide tiles; CTA pairs (256 x 256 tiles
+    over 256-row segments)."""
     shape = REDUCED[name]
     case = G.float_case(shape)
     run = G.run_gpu(case, **G.MODES[mode])
@@ -210,14 +211,14 @@ def test_masked_slots_and_duplicates():
     G.assert_close(G.out_f64(G.run_gpu(case)), G.oracle_out(case), "mxfp8", "masked/dup")
 
 
-@pytest.mark.parametrize("cta", ["single", "pair"])
+@pytest.mark.parametrize("mode", ["fused", "split256", "pair"])
 @pytest.mark.parametrize("fmt", ["bf16", "nvfp4"])
-def test_all_tokens_one_expert(fmt, cta):
+def test_all_tokens_one_expert(fmt, mode):
     shape = _small_case(fmt, T=300, k=1)
     ids = np.full((300, 1), 5, np.int32)
     w = np.ones((300, 1), np.float32)
     case = G.float_case(shape, ids=ids, w=w)
-    run = G.run_gpu(case, cta=cta)
+    run = G.run_gpu(case, **G.MODES[mode])
     G.assert_close(G.out_f64(run), G.oracle_out(case), fmt, "one expert")
     off = G.region_i32(run, 300, "offsets")[:9]
     pad = 384 if run.plan.block_m(300) == 128 else 512
@@ -267,13 +268,13 @@ def test_workspace_too_small():
     assert e.value.status == 4
 
 
-@pytest.mark.parametrize("cta", ["single", "pair"])
+@pytest.mark.parametrize("mode", ["fused", "split256", "pair"])
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
-def test_deterministic(fmt, cta):
+def test_deterministic(fmt, mode):
     shape = _small_case(fmt, T=150, k=4, E=8)
     case = G.float_case(shape)
-    a = G.run_gpu(case, cta=cta).out.clone()
-    b = G.run_gpu(case, cta=cta).out.clone()
+    a = G.run_gpu(case, **G.MODES[mode]).out.clone()
+    b = G.run_gpu(case, **G.MODES[mode]).out.clone()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
@@ -375,14 +376,14 @@ def test_weight_transform_layout(fmt):
 
 # ----------------------------------------------------------------------------- failure detection
 
-@pytest.mark.parametrize("cta", ["single", "pair"])
-def test_bounded_wait_timeout_reports_and_context_survives(cta):
+@pytest.mark.parametrize("mode", ["fused", "split256", "pair"])
+def test_bounded_wait_timeout_reports_and_context_survives(mode):
     """A 1 ns limit makes the GEMM's pipeline waits run out: the kernel records
     MOE_ERR_TIMEOUT, waits for its own copies and MMAs, and returns. The status reads
     back, and the same plan with the default limit then computes the same answer."""
     shape = _small_case("mxfp8", T=256, H=2048, I=512, E=4, k=2)
     case = G.float_case(shape)
-    run = G.run_gpu(case, cta=cta)
+    run = G.run_gpu(case, **G.MODES[mode])
     good = G.out_f64(run)
     run.plan.set_wait_timeout(1)
     run.plan.forward(run.inputs["hidden"], run.inputs["topk_ids"], run.inputs["topk_weights"], run.kweights,
