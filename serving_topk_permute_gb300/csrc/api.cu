@@ -543,6 +543,7 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
     da.H = d.H;
     da.k = d.k;
     da.inv = (const int*)R(R_INV);
+    da.src = (int*)R(R_SRC);
     da.fmt = d.fmt;
     da.xq = R(R_XQ);
     da.xsf = R(R_XSF);

@@ -45,12 +45,15 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 4) combine_kernel(const Combi
     __shared__ int s_rows[32];
     __shared__ float s_w[32];
     __shared__ float s_red[COMBINE_THREADS / 32];
-    grid_dep_wait();  // the L2 GEMM (and the shared expert) have written y
-    grid_dep_launch();
+    // inv_perm (routing) and the weights (an input) are complete before this kernel starts:
+    // every kernel of the forward lets its successor start only after its own wait, so
+    // routing finished before the GEMM did its wait. y is read after the wait.
     if (tid < a.k) {
-        s_rows[tid] = a.inv[(int64_t)t * a.k + tid];
-        s_w[tid] = a.w[(int64_t)t * a.k + tid];
+        s_rows[tid] = __ldcg(a.inv + (int64_t)t * a.k + tid);  // from L2: no stale L1 line
+        s_w[tid] = __ldcg(a.w + (int64_t)t * a.k + tid);
     }
+    grid_dep_wait();  // the GEMMs have written y (and the shared expert ys)
+    grid_dep_launch();
     __syncthreads();
     const bool norm = a.gamma != nullptr;
     uint4* orow = reinterpret_cast<uint4*>(a.out + (int64_t)t * a.H);

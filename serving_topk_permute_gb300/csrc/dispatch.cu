@@ -66,17 +66,16 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
     __shared__ int s_rows[32];
     __shared__ float s_amax[DISPATCH_THREADS / 32];
 
-    grid_dep_wait();  // routing has written inv
-    grid_dep_launch();
-    if (tid < a.k) s_rows[tid] = a.inv[(int64_t)t * a.k + tid];
-
+    // The token's row and its own scale do not depend on routing. The hidden states are
+    // complete before this kernel starts (routing, the kernel before it, lets it start only
+    // after its own wait for its predecessor), so they are read while routing still runs.
     // load the token's row into registers
     uint4 v[DISPATCH_MAX_CHUNKS];
     const uint4* xrow = reinterpret_cast<const uint4*>(a.x + (int64_t)t * a.H);
 #pragma unroll
     for (int i = 0; i < DISPATCH_MAX_CHUNKS; ++i) {
         const int c = tid + i * DISPATCH_THREADS;
-        v[i] = c < nchunks ? xrow[c] : make_uint4(0, 0, 0, 0);
+        v[i] = c < nchunks ? __ldcg(xrow + c) : make_uint4(0, 0, 0, 0);  // from L2: no stale L1 line
     }
 
     // NVFP4: the token's own scale
@@ -98,10 +97,16 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
 #pragma unroll
         for (int w = 1; w < DISPATCH_THREADS / 32; ++w) amax = fmaxf(amax, s_amax[w]);
         gs = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
-        if (tid == 0) a.x_scale[t] = gs;
-    } else {
-        __syncthreads();
     }
+    grid_dep_wait();  // routing has written inv (and the previous forward no longer reads x_scale)
+    grid_dep_launch();
+    if (a.fmt == MOE_FMT_NVFP4 && tid == 0) a.x_scale[t] = gs;
+    if (tid < a.k) {
+        const int r = a.inv[(int64_t)t * a.k + tid];
+        s_rows[tid] = r;
+        if (r >= 0) a.src[r] = t * a.k + tid;  // the routing kernel wrote the padding rows
+    }
+    __syncthreads();
     const int k = a.k;
     const int64_t nks_x = fmt_k_stages(a.fmt, a.H);
 

@@ -38,6 +38,7 @@ struct FusedCfg {
     static constexpr int NB = BN / NBLK;
     static constexpr int STAGES = 4;
     static constexpr int TRING = 4;                     // tile indices in flight between the warps
+    static constexpr int PREFETCH_STAGES = 4;           // weight stages of the first tile pulled into L2 early
     static constexpr int A_BYTES = BM * BK_BYTES;
     static constexpr int B_BYTES = BN * BK_BYTES;
     static constexpr int SFA_BYTES = S * ATOM_BYTES;
@@ -62,6 +63,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                      const GemmArgs p1, const GemmArgs p2, const FusedSched fs) {
     using C = FusedCfg<FMT>;
     constexpr int S = C::S, NB = C::NB, STAGES = C::STAGES, BN = C::BN, TRING = C::TRING;
+    constexpr int PREFETCH_STAGES = C::PREFETCH_STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
@@ -107,13 +109,29 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    grid_dep_wait();  // the set-up above overlaps the previous kernel; everything below reads its output
-    grid_dep_launch();
 
-    const int m_tiles = p1.m_tiles_dev ? *p1.m_tiles_dev : p1.m_tiles_host;
+    // What the routing kernel wrote (the row-tile count and experts, the zeroed tile
+    // counter) is complete before this kernel starts, even while the kernel just before
+    // it (dispatch) still runs: every kernel of the forward lets its successor start
+    // only after its own grid-dependency wait, so by then routing has finished. So the
+    // producer takes its first tile and starts pulling that tile's first weight stages
+    // into L2 before the wait, overlapping the previous kernel. (Loads bypass L1.)
+    const int m_tiles = p1.m_tiles_dev ? __ldcg(p1.m_tiles_dev) : p1.m_tiles_host;
     const int total1 = m_tiles * p1.n_tiles;
     const int total = total1 + m_tiles * p2.n_tiles;
     const uint32_t done_target = (uint32_t)(EPI_WARPS * p1.n_tiles);
+    int first = -1;
+    if (warp == 0 && lane == 0) {
+        first = (int)atomicAdd(fs.counter, 1u);
+        if (first < total1) {
+            const int mt = first / p1.n_tiles, nt = first % p1.n_tiles;
+            const int e = p1.tile_expert ? __ldcg(p1.tile_expert + mt) : 0;
+            for (int ks = 0; ks < p1.nks && ks < PREFETCH_STAGES; ++ks)
+                tma_prefetch_3d(&tmB1, ks * BK_BYTES, nt * BN, e);
+        }
+    }
+    grid_dep_wait();  // everything below may read the previous kernel's output
+    grid_dep_launch();
 
     auto give_up = [&]() {
         set_error(p1.err, MOE_ERR_TIMEOUT);
@@ -135,7 +153,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             int last_parity[STAGES];
 #pragma unroll
             for (int s = 0; s < STAGES; ++s) last_parity[s] = -1;
-            int next = (int)atomicAdd(fs.counter, 1u);
+            int next = first;
             for (int k = 0;; ++k) {
                 const int t = next;
                 const int r = k % TRING;

@@ -41,7 +41,8 @@ struct LaunchAttrs {
 
 // ------------------------------------------------------------------ routing
 // Histogram, BLOCK_M (bm)-padded offsets, stable scatter (one CTA). Writes cnt[E],
-// off[E+1], src[M_pad] (-1 padding), inv[T*k] (-1 masked), tile_expert[M_pad/bm],
+// off[E+1], src[r] = -1 for the padding rows only (the routed rows are src[inv[s]] = s,
+// written by the dispatch kernel), inv[T*k] (-1 masked), tile_expert[M_pad/bm],
 // meta[0] = M_pad, meta[1] = M_pad / bm.
 size_t route_smem_bytes(int E);
 cudaError_t route_prepare(int E);   // sets the dynamic shared memory attribute (E <= 512)
@@ -55,6 +56,7 @@ struct DispatchArgs {
     const uint16_t* x;   // bf16 bits [T, H]
     int T, H, k;
     const int* inv;      // [T*k] permuted row of each slot (-1 = masked)
+    int* src;            // [M_pad] written here for the routed rows: src[inv[s]] = s
     int fmt;             // routed format
     uint8_t* xq;         // [M_pad_max, H/vpe] permuted rows
     uint8_t* xsf;        // scale atoms

@@ -7,13 +7,17 @@
 // One CTA of 1024 threads (32 warps). Warp w owns a contiguous chunk of the
 // flat slots s = t*k + j.
 //   pass 1  each warp counts its chunk per expert into its own shared row
-//   scan    per expert: exclusive prefix over warps (a warp's base inside the
-//           expert) and the total; padded sizes; a block-wide scan gives the
-//           segment offsets
+//   scan    per expert, one warp by shuffles: exclusive prefix over the 32 warps'
+//           counts (a warp's base inside the expert) and the total; padded
+//           sizes; a block-wide scan gives the segment offsets; the padding rows
+//           are marked -1
 //   pass 2  each warp walks its chunk in ascending order, 32 slots at a time;
 //           __match_any_sync groups lanes with the same expert, the rank inside
-//           the group plus the warp's running count gives the row. Rows inside
-//           a segment are therefore ordered by ascending slot: a stable scatter.
+//           the group plus the warp's running count gives the row, stored as
+//           inv_perm[slot] (coalesced). Rows inside a segment are therefore
+//           ordered by ascending slot: a stable scatter. The inverse, src[row],
+//           is written by the dispatch kernel, one token's slots per CTA: as
+//           scattered 4-byte stores from this one CTA it took most of the time.
 // Integer-only and deterministic. Ids outside [-1, E) set MOE_ERR_BAD_EXPERT_ID
 // and are treated as masked.
 #include "common.cuh"
@@ -30,8 +34,9 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
                  int* __restrict__ off, int* __restrict__ src, int* __restrict__ inv, int* __restrict__ tile_expert,
                  int* __restrict__ meta, int* err, uint32_t* __restrict__ zero, int n_zero) {
     extern __shared__ int sm[];
-    int* wcnt = sm;                          // [32][E]: per-warp counts, then per-warp running bases
-    int* s_off = sm + ROUTE_WARPS * E;       // [E+1]
+    const int WS = E | 1;                    // odd row stride: a warp reading one expert's 32 rows hits 32 banks
+    int* wcnt = sm;                          // [32][WS]: per-warp counts, then per-warp running bases
+    int* s_off = sm + ROUTE_WARPS * WS;      // [E+1]
     int* s_cnt = s_off + (E + 1);            // [E]
     int* s_wsum = s_cnt + E;                 // [32] scan scratch
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -39,43 +44,52 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     const int chunk = (int)align_up(ceil_div(R, ROUTE_WARPS), 32);
     const int beg = min(warp * chunk, R), end = min(beg + chunk, R);
 
-    for (int i = tid; i < ROUTE_WARPS * E; i += ROUTE_THREADS) wcnt[i] = 0;
+    for (int i = tid; i < ROUTE_WARPS * WS; i += ROUTE_THREADS) wcnt[i] = 0;
     grid_dep_wait();  // the previous kernel (which may still read src / inv) has finished
     grid_dep_launch();
     if (tid == 0 && err) *err = 0;  // the status word reflects this forward only
     for (int i = tid; i < n_zero; i += ROUTE_THREADS) zero[i] = 0u;
     __syncthreads();
 
-    // pass 1: per-warp histograms (ids loaded RB groups of 32 at a time: independent loads in flight)
+    // pass 1: per-warp histograms (ids loaded RB groups of 32 at a time: independent loads in
+    // flight). A warp whose chunk is one batch keeps its ids in registers for pass 2.
+    const bool one_batch = end - beg <= 32 * RB;
+    int kept[RB];
     for (int s0 = beg; s0 < end; s0 += 32 * RB) {
         int ev[RB];
 #pragma unroll
         for (int u = 0; u < RB; ++u) {
             const int s = s0 + 32 * u + lane;
             ev[u] = s < end ? ids[s] : -1;
+            kept[u] = ev[u];
         }
 #pragma unroll
         for (int u = 0; u < RB; ++u) {
             if (s0 + 32 * u >= end) break;  // warp-uniform
             const int e = ev[u];
             if (e >= 0 && e < E)
-                atomicAdd(&wcnt[warp * E + e], 1);
+                atomicAdd(&wcnt[warp * WS + e], 1);
             else if (e != -1)
                 set_error(err, MOE_ERR_BAD_EXPERT_ID);
         }
     }
     __syncthreads();
 
-    // per expert: exclusive prefix over warps, total, padded size
-    for (int e = tid; e < E; e += ROUTE_THREADS) {
-        int run = 0;
-        for (int w = 0; w < ROUTE_WARPS; ++w) {
-            const int c = wcnt[w * E + e];
-            wcnt[w * E + e] = run;
-            run += c;
+    // per expert (one warp each): exclusive prefix of its 32 per-warp counts by shuffles,
+    // the total, and the padded size
+    for (int e = warp; e < E; e += ROUTE_WARPS) {
+        const int c = wcnt[lane * WS + e];
+        int x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
         }
-        s_cnt[e] = run;
-        cnt[e] = run;
+        wcnt[lane * WS + e] = x - c;
+        if (lane == 31) {
+            s_cnt[e] = x;
+            cnt[e] = x;
+        }
     }
     __syncthreads();
 
@@ -106,18 +120,19 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     }
     __syncthreads();
     for (int e = tid; e <= E; e += ROUTE_THREADS) off[e] = s_off[e];
-    // every row starts as padding (-1); the scatter below overwrites the routed ones
-    for (int r = tid; r < s_off[E]; r += ROUTE_THREADS) src[r] = -1;
-    __syncthreads();
+    // the padding rows of each segment (one warp per expert); the scatter below writes the rest
+    for (int e = warp; e < E; e += ROUTE_WARPS)
+        for (int r = s_off[e] + s_cnt[e] + lane; r < s_off[e + 1]; r += 32) src[r] = -1;
 
-    // pass 2: stable scatter, in ascending slot order (ids again loaded RB groups at a time)
+    // pass 2: stable scatter, in ascending slot order (ids again loaded RB groups at a time,
+    // unless still in registers)
     const unsigned lt = (1u << lane) - 1u;
     for (int s0 = beg; s0 < end; s0 += 32 * RB) {
         int ev[RB];
 #pragma unroll
         for (int u = 0; u < RB; ++u) {
             const int s = s0 + 32 * u + lane;
-            ev[u] = s < end ? ids[s] : -1;
+            ev[u] = one_batch ? kept[u] : (s < end ? ids[s] : -1);
         }
 #pragma unroll
         for (int u = 0; u < RB; ++u) {
@@ -127,15 +142,9 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
             const bool routed = s < end && e >= 0 && e < E;
             const int key = routed ? e : E + lane;  // unrouted lanes never group
             const unsigned peers = __match_any_sync(0xffffffffu, key);
-            if (routed) {
-                const int row = s_off[e] + wcnt[warp * E + e] + __popc(peers & lt);
-                src[row] = s;
-                inv[s] = row;
-            } else if (s < end) {
-                inv[s] = -1;
-            }
+            if (s < end) inv[s] = routed ? s_off[e] + wcnt[warp * WS + e] + __popc(peers & lt) : -1;
             __syncwarp();
-            if (routed && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+            if (routed && lane == __ffs(peers) - 1) wcnt[warp * WS + e] += __popc(peers);
             __syncwarp();
         }
     }
@@ -149,7 +158,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     }
 }
 
-size_t route_smem_bytes(int E) { return sizeof(int) * ((size_t)ROUTE_WARPS * E + (E + 1) + E + 32); }
+size_t route_smem_bytes(int E) { return sizeof(int) * ((size_t)ROUTE_WARPS * (E | 1) + (E + 1) + E + 32); }
 
 cudaError_t route_prepare(int E) {
     return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)route_smem_bytes(E));
