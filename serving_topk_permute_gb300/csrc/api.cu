@@ -79,7 +79,7 @@ int block_m_for(const moe_config_t& c, int T) { return use_pair(c, routed_rows_p
 // ------------------------------------------------------------------ workspace layout
 enum Region {
     R_ERR, R_META, R_CNT, R_OFF, R_TILE_EXPERT, R_SRC, R_INV, R_XSCALE, R_XQ, R_XSF, R_HQ, R_HSF, R_Y, R_HDBG,
-    R_SXQ, R_SXSF, R_SHQ, R_SHSF, R_SY, R_SCHED, R_COUNT
+    R_SXQ, R_SXSF, R_SHQ, R_SHSF, R_SY, R_SCHED, R_WBASE, R_COUNT
 };
 
 struct Layout {
@@ -126,6 +126,7 @@ Layout layout_of(const moe_config_t& c, int T) {
     // schedule counters of the one-kernel GEMM: routed (counter, done[m_tiles_max]),
     // then shared (counter, done[t_pad / 128]); zeroed by the routing kernel
     sz[R_SCHED] = 4 * (2 + L.m_tiles_max + L.t_pad / BM);
+    sz[R_WBASE] = 4 * ROUTE_WARPS * d.E;  // each routing chunk's first row in each expert
     int64_t o = 0;
     for (int r = 0; r < R_COUNT; ++r) {
         L.off[r] = o;
@@ -535,14 +536,17 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
         KernelTimer kt(plan, MOE_KERNEL_ROUTE, st);
         CUDA_TRY(launch_route(topk_ids, T, d.k, d.E, bm, (int*)R(R_CNT), (int*)R(R_OFF), (int*)R(R_SRC), (int*)R(R_INV),
                           (int*)R(R_TILE_EXPERT), meta, err, st, plan->pdl, (uint32_t*)R(R_SCHED),
-                          (int)(L.size[R_SCHED] / 4)));
+                          (int)(L.size[R_SCHED] / 4), (int*)R(R_WBASE)));
     }
     DispatchArgs da{};
     da.x = (const uint16_t*)hidden;
     da.T = T;
     da.H = d.H;
     da.k = d.k;
-    da.inv = (const int*)R(R_INV);
+    da.ids = topk_ids;
+    da.E = d.E;
+    da.wbase = (const int*)R(R_WBASE);
+    da.inv = (int*)R(R_INV);
     da.src = (int*)R(R_SRC);
     da.fmt = d.fmt;
     da.xq = R(R_XQ);

@@ -38,6 +38,12 @@ __host__ __device__ inline int64_t fmt_row_bytes(int fmt, int64_t K) { return K 
 // number of 128-byte K stages for K elements
 __host__ __device__ inline int64_t fmt_k_stages(int fmt, int64_t K) { return fmt_row_bytes(fmt, K) / BK_BYTES; }
 
+// The routing kernel splits the flat slots s = t*k + j into ROUTE_WARPS contiguous
+// chunks, one per warp; a slot's rank inside its expert is the chunk's base for the
+// expert plus the number of equal ids before it in the chunk.
+constexpr int ROUTE_WARPS = 32;
+__host__ __device__ inline int route_chunk(int64_t R) { return (int)(((R + ROUTE_WARPS - 1) / ROUTE_WARPS + 31) / 32 * 32); }
+
 // Byte offset of scale block kb of row r in an activation scale-atom array laid
 // out [row tile][K stage][S atoms][512]: within an atom, row m = 32j + i and
 // scale b (of 4) sit at byte 16i + 4j + b.

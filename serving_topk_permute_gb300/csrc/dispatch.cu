@@ -19,6 +19,8 @@
 // the scale bytes to the matching position of the 128-row scale atoms the MMA
 // reads. With a shared expert, the token is also quantised to the shared format
 // into row t of a separate (unpermuted) buffer.
+#include <climits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -58,12 +60,14 @@ __device__ __forceinline__ int mxfp8_block_exponent(const float (&f)[8]) {
     return ue8m0_exponent(amax);
 }
 
-__global__ void __launch_bounds__(DISPATCH_THREADS)
+__global__ void __launch_bounds__(DISPATCH_THREADS, 3)
     dispatch_kernel(const DispatchArgs a) {
     const int t = blockIdx.x;
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     const int nchunks = a.H / 8;
     __shared__ int s_rows[32];
+    __shared__ int s_rank[32];  // rank of slot j among the equal ids before it in its routing chunk
+    __shared__ int s_exp[32];
     __shared__ float s_amax[DISPATCH_THREADS / 32];
 
     // The token's row and its own scale do not depend on routing. The hidden states are
@@ -76,6 +80,50 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
     for (int i = 0; i < DISPATCH_MAX_CHUNKS; ++i) {
         const int c = tid + i * DISPATCH_THREADS;
         v[i] = c < nchunks ? __ldcg(xrow + c) : make_uint4(0, 0, 0, 0);  // from L2: no stale L1 line
+    }
+
+    // Each slot's row is its routing chunk's first row in the expert (written by the
+    // routing kernel) plus the number of equal ids before it in the chunk: a stable
+    // scatter, counted here from the ids alone. The CTA scans the chunk's ids before this
+    // token once (128-bit loads, 8 ids per thread per round), counting the token's k
+    // experts, then adds the equal slots of the token itself that come first. (When k
+    // does not divide 32 a token's slots may straddle two chunks; a slot in the second
+    // chunk counts only the token's slots from that chunk's start.)
+    const int R = a.T * a.k, chunk = route_chunk(R);
+    const int s0 = t * a.k, c0 = s0 / chunk * chunk;
+    if (tid < a.k) {
+        s_exp[tid] = __ldcg(a.ids + s0 + tid);
+        s_rank[tid] = 0;
+    }
+    __syncthreads();
+    for (int base = c0; base < s0; base += 8 * DISPATCH_THREADS) {
+        int v[8];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int i0 = base + 4 * tid + 4 * DISPATCH_THREADS * m;
+            if (i0 + 3 < s0) {
+                const int4 q = __ldcg(reinterpret_cast<const int4*>(a.ids + i0));
+                v[4 * m] = q.x, v[4 * m + 1] = q.y, v[4 * m + 2] = q.z, v[4 * m + 3] = q.w;
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[4 * m + u] = i0 + u < s0 ? __ldcg(a.ids + i0 + u) : INT_MIN;
+            }
+        }
+        for (int j = 0; j < a.k; ++j) {
+            const int e = s_exp[j];
+            int n = 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) n += v[u] == e;
+            n = __reduce_add_sync(0xffffffffu, n);
+            if (lane == 0 && n) atomicAdd(&s_rank[j], n);
+        }
+    }
+    __syncthreads();
+    if (tid < a.k) {
+        const int e = s_exp[tid], my_chunk = (s0 + tid) / chunk;
+        int n = my_chunk == s0 / chunk ? s_rank[tid] : 0;
+        for (int j = 0; j < tid; ++j) n += s_exp[j] == e && (s0 + j) / chunk == my_chunk;
+        s_rank[tid] = n;  // only this thread reads it back (after the next barrier)
     }
 
     // NVFP4: the token's own scale
@@ -98,13 +146,15 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
         for (int w = 1; w < DISPATCH_THREADS / 32; ++w) amax = fmaxf(amax, s_amax[w]);
         gs = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
     }
-    grid_dep_wait();  // routing has written inv (and the previous forward no longer reads x_scale)
+    grid_dep_wait();  // routing has written the chunk bases (and the previous forward is done with x_scale)
     grid_dep_launch();
     if (a.fmt == MOE_FMT_NVFP4 && tid == 0) a.x_scale[t] = gs;
     if (tid < a.k) {
-        const int r = a.inv[(int64_t)t * a.k + tid];
+        const int s = t * a.k + tid, e = s_exp[tid];
+        const int r = e >= 0 && e < a.E ? a.wbase[s / chunk * a.E + e] + s_rank[tid] : -1;
+        a.inv[s] = r;
         s_rows[tid] = r;
-        if (r >= 0) a.src[r] = t * a.k + tid;  // the routing kernel wrote the padding rows
+        if (r >= 0) a.src[r] = s;  // the routing kernel wrote the padding rows
     }
     __syncthreads();
     const int k = a.k;

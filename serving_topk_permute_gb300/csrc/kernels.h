@@ -46,16 +46,22 @@ struct LaunchAttrs {
 // meta[0] = M_pad, meta[1] = M_pad / bm.
 size_t route_smem_bytes(int E);
 cudaError_t route_prepare(int E);   // sets the dynamic shared memory attribute (E <= 512)
-// zero[0..n_zero): words the routing kernel also zeroes (the GEMM schedule counters)
+// zero[0..n_zero): words the routing kernel also zeroes (the GEMM schedule counters).
+// With wbase ([ROUTE_WARPS][E] ints), the kernel writes each slot chunk's first row in
+// each expert there and leaves inv (and the routed rows of src) to the dispatch kernel;
+// without it, it writes inv itself.
 cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int bm, int* cnt, int* off, int* src, int* inv,
                          int* tile_expert, int* meta, int* err, cudaStream_t st, bool pdl = false,
-                         uint32_t* zero = nullptr, int n_zero = 0);
+                         uint32_t* zero = nullptr, int n_zero = 0, int* wbase = nullptr);
 
 // ------------------------------------------------------------------ dispatch quantisation
 struct DispatchArgs {
     const uint16_t* x;   // bf16 bits [T, H]
     int T, H, k;
-    const int* inv;      // [T*k] permuted row of each slot (-1 = masked)
+    const int32_t* ids;  // [T*k] expert of each slot
+    int E;
+    const int* wbase;    // [ROUTE_WARPS][E] first row of each slot chunk in each expert (routing)
+    int* inv;            // [T*k] written here: permuted row of each slot (-1 = masked)
     int* src;            // [M_pad] written here for the routed rows: src[inv[s]] = s
     int fmt;             // routed format
     uint8_t* xq;         // [M_pad_max, H/vpe] permuted rows

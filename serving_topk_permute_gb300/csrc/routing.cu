@@ -25,14 +25,14 @@
 
 namespace moe {
 
-constexpr int ROUTE_THREADS = 1024;
-constexpr int ROUTE_WARPS = ROUTE_THREADS / 32;
+constexpr int ROUTE_THREADS = 32 * ROUTE_WARPS;
 constexpr int RB = 8;  // 32-slot groups whose ids are loaded together
 
 __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     route_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int bm, int* __restrict__ cnt,
                  int* __restrict__ off, int* __restrict__ src, int* __restrict__ inv, int* __restrict__ tile_expert,
-                 int* __restrict__ meta, int* err, uint32_t* __restrict__ zero, int n_zero) {
+                 int* __restrict__ meta, int* err, uint32_t* __restrict__ zero, int n_zero,
+                 int* __restrict__ wbase, bool scatter) {
     extern __shared__ int sm[];
     const int WS = E | 1;                    // odd row stride: a warp reading one expert's 32 rows hits 32 banks
     int* wcnt = sm;                          // [32][WS]: per-warp counts, then per-warp running bases
@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     int* s_wsum = s_cnt + E;                 // [32] scan scratch
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int R = T * k;
-    const int chunk = (int)align_up(ceil_div(R, ROUTE_WARPS), 32);
+    const int chunk = route_chunk(R);
     const int beg = min(warp * chunk, R), end = min(beg + chunk, R);
 
     for (int i = tid; i < ROUTE_WARPS * WS; i += ROUTE_THREADS) wcnt[i] = 0;
@@ -120,6 +120,11 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     }
     __syncthreads();
     for (int e = tid; e <= E; e += ROUTE_THREADS) off[e] = s_off[e];
+    // each chunk's first row in each expert (its base); the dispatch kernel adds a slot's
+    // rank inside the chunk
+    if (wbase)
+        for (int i = tid; i < ROUTE_WARPS * E; i += ROUTE_THREADS)
+            wbase[i] = s_off[i % E] + wcnt[(i / E) * WS + i % E];
     // the padding rows of each segment (one warp per expert); the scatter below writes the rest
     for (int e = warp; e < E; e += ROUTE_WARPS)
         for (int r = s_off[e] + s_cnt[e] + lane; r < s_off[e + 1]; r += 32) src[r] = -1;
@@ -127,7 +132,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     // pass 2: stable scatter, in ascending slot order (ids again loaded RB groups at a time,
     // unless still in registers)
     const unsigned lt = (1u << lane) - 1u;
-    for (int s0 = beg; s0 < end; s0 += 32 * RB) {
+    for (int s0 = beg; scatter && s0 < end; s0 += 32 * RB) {
         int ev[RB];
 #pragma unroll
         for (int u = 0; u < RB; ++u) {
@@ -166,11 +171,11 @@ cudaError_t route_prepare(int E) {
 
 cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int bm, int* cnt, int* off, int* src, int* inv,
                          int* tile_expert, int* meta, int* err, cudaStream_t st, bool pdl, uint32_t* zero,
-                         int n_zero) {
+                         int n_zero, int* wbase) {
     LaunchAttrs at(pdl);
     cudaLaunchConfig_t cfg = at.config(dim3(1), dim3(ROUTE_THREADS), route_smem_bytes(E), st);
     return cudaLaunchKernelEx(&cfg, route_kernel, ids, T, k, E, bm, cnt, off, src, inv, tile_expert, meta, err, zero,
-                              n_zero);
+                              n_zero, wbase, wbase == nullptr);
 }
 
 }  // namespace moe
