@@ -1,4 +1,4 @@
-"""Oracle number formats: E2M1, E4M3, UE8M0, BF16 and the MXFP8 / NVFP4 quantisers.
+"""Oracle number formats: E2M1, E4M3, UE8M0, BF16 and the MXFP8 / MXFP4 / NVFP4 quantisers.
 
 TEST INFRASTRUCTURE ONLY. Nothing in the product path imports this module;
 only tests, the smoke check and the benchmark's CPU-baseline leg do.
@@ -16,7 +16,10 @@ finite magnitude. Pages are silent on:
     element 2i+1 the high nibble;
   * the NVFP4 scale arithmetic: the plain two-level recipe in fp32 (see
     ``nvfp4_quantize``), whose global scale is amax / (448 * 6);
-  * the UE8M0 byte of an all-zero block: 127 (scale 1.0).
+  * the UE8M0 byte of an all-zero block: 127 (scale 1.0);
+  * the MX block exponent: the smallest e with amax <= (largest element value) * 2^e,
+    i.e. 2^ceil(log2(amax / 448)) for MXFP8 (as the MXFP8 workloads state) and,
+    by the same rule, 2^ceil(log2(amax / 6)) for MXFP4, so no element saturates.
 """
 from __future__ import annotations
 
@@ -135,18 +138,23 @@ def bf16_bits(v) -> np.ndarray:
 MX_BLOCK = 32
 
 
-def ue8m0_exponent(amax) -> np.ndarray:
-    """The smallest integer e with amax <= 448 * 2^e (i.e. ceil(log2(amax / 448))),
+def mx_exponent(amax, vmax: float) -> np.ndarray:
+    """The smallest integer e with amax <= vmax * 2^e (i.e. ceil(log2(amax / vmax))),
     decided exactly against that inequality; 0 for amax == 0; clamped to [-127, 127]."""
     amax = np.asarray(amax, dtype=np.float64)
     pos = amax > 0
-    safe = np.where(pos, amax, E4M3_MAX)
-    e = np.ceil(np.log2(safe / E4M3_MAX)).astype(np.int64)
+    safe = np.where(pos, amax, vmax)
+    e = np.ceil(np.log2(safe / vmax)).astype(np.int64)
     for _ in range(3):                                   # exact fix-up of the float log2
-        e = np.where(safe > np.ldexp(E4M3_MAX, e), e + 1, e)
-        e = np.where(safe <= np.ldexp(E4M3_MAX, e - 1), e - 1, e)
+        e = np.where(safe > np.ldexp(vmax, e), e + 1, e)
+        e = np.where(safe <= np.ldexp(vmax, e - 1), e - 1, e)
     e = np.where(pos, e, 0)
     return np.clip(e, -127, 127)
+
+
+def ue8m0_exponent(amax) -> np.ndarray:
+    """MXFP8 block exponent: the smallest integer e with amax <= 448 * 2^e."""
+    return mx_exponent(amax, E4M3_MAX)
 
 
 def mxfp8_quantize(x) -> tuple[np.ndarray, np.ndarray]:
@@ -169,6 +177,35 @@ def mxfp8_dequantize(codes, sf) -> np.ndarray:
     codes = np.asarray(codes, dtype=np.uint8)
     K = codes.shape[-1]
     v = E4M3_TABLE[codes].reshape(codes.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
+    return (v * UE8M0_TABLE[np.asarray(sf, dtype=np.uint8)][..., None]).reshape(codes.shape)
+
+
+# ----------------------------------------------------------------------------- MXFP4 (E2M1 + UE8M0 per 1x32)
+
+E2M1_MAX = 6.0
+
+
+def mxfp4_quantize(x) -> tuple[np.ndarray, np.ndarray]:
+    """Quantise rows of x (last axis K, a multiple of 32) to MXFP4.
+
+    Per 1x32 block: e = the smallest integer with amax <= 6 * 2^e, code = E2M1(x * 2^-e)
+    (nearest, ties to even), scale byte = e + 127. Returns (codes packed two per byte,
+    element 2i in the low nibble, u8 [..., K/2]; scale bytes u8 [..., K/32]).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    K = x.shape[-1]
+    if K % MX_BLOCK:
+        raise ValueError("mxfp4_quantize: K must be a multiple of 32")
+    xb = x.reshape(x.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
+    e = mx_exponent(np.abs(xb).max(axis=-1), E2M1_MAX)
+    codes = e2m1_encode(xb * np.ldexp(1.0, -e)[..., None])
+    return pack_e2m1(codes.reshape(x.shape)), (e + 127).astype(np.uint8)
+
+
+def mxfp4_dequantize(packed, sf) -> np.ndarray:
+    codes = unpack_e2m1(packed)
+    K = codes.shape[-1]
+    v = E2M1_TABLE[codes].reshape(codes.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
     return (v * UE8M0_TABLE[np.asarray(sf, dtype=np.uint8)][..., None]).reshape(codes.shape)
 
 

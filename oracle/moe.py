@@ -33,7 +33,7 @@ import numpy as np
 from . import formats as F
 from .routing import permute
 
-BF16, MXFP8, NVFP4 = "bf16", "mxfp8", "nvfp4"
+BF16, MXFP8, NVFP4, MXFP4 = "bf16", "mxfp8", "nvfp4", "mxfp4"
 
 
 @dataclass
@@ -73,6 +73,8 @@ class ExpertWeights:
             return F.bf16_bits_to_f64(codes)
         if self.fmt == MXFP8:
             return F.mxfp8_dequantize(codes, sf)
+        if self.fmt == MXFP4:
+            return F.mxfp4_dequantize(codes, sf)
         return F.nvfp4_dequantize(codes, sf, gs)
 
     def w13_of(self, e: int) -> np.ndarray:
@@ -100,6 +102,10 @@ def quantize_weights(fmt: str, w13_f, w2_f) -> ExpertWeights:
         c13, s13 = F.mxfp8_quantize(w13_f)
         c2, s2 = F.mxfp8_quantize(w2_f)
         return ExpertWeights(MXFP8, c13, c2, s13, s2)
+    if fmt == MXFP4:
+        c13, s13 = F.mxfp4_quantize(w13_f)
+        c2, s2 = F.mxfp4_quantize(w2_f)
+        return ExpertWeights(MXFP4, c13, c2, s13, s2)
     E = w13_f.shape[0]
     gs13 = F.nvfp4_global_scale(np.abs(w13_f).reshape(E, -1).max(axis=1))
     gs2 = F.nvfp4_global_scale(np.abs(w2_f).reshape(E, -1).max(axis=1))
@@ -120,14 +126,17 @@ class Dispatched:
 
 
 def dispatch_quantize(x_bits, fmt: str) -> Dispatched:
-    """Quantise each token once (bf16: no change; MXFP8: 1x32 UE8M0; NVFP4: per-token
-    fp32 scale amax/2688, then 1x16 E4M3 block scales)."""
+    """Quantise each token once (bf16: no change; MXFP8 / MXFP4: 1x32 UE8M0; NVFP4:
+    per-token fp32 scale amax/2688, then 1x16 E4M3 block scales)."""
     x = F.bf16_bits_to_f64(x_bits)
     if fmt == BF16:
         return Dispatched(BF16, x)
     if fmt == MXFP8:
         codes, sf = F.mxfp8_quantize(x)
         return Dispatched(MXFP8, F.mxfp8_dequantize(codes, sf), codes, sf)
+    if fmt == MXFP4:
+        codes, sf = F.mxfp4_quantize(x)
+        return Dispatched(MXFP4, F.mxfp4_dequantize(codes, sf), codes, sf)
     gs = F.nvfp4_global_scale(np.abs(x).max(axis=1).astype(np.float32))
     codes, sf = F.nvfp4_quantize(x, gs)
     return Dispatched(NVFP4, F.nvfp4_dequantize(codes, sf, gs), codes, sf, gs)
@@ -140,6 +149,8 @@ def l2_input_quantize(h, fmt: str, a2: float | None = None) -> np.ndarray:
         return F.bf16_round(h32)
     if fmt == MXFP8:
         return F.mxfp8_dequantize(*F.mxfp8_quantize(h32))
+    if fmt == MXFP4:
+        return F.mxfp4_dequantize(*F.mxfp4_quantize(h32))
     gs = np.float32(a2)
     codes, sf = F.nvfp4_quantize(h32, gs)
     return F.nvfp4_dequantize(codes, sf, gs)
@@ -152,6 +163,8 @@ def l2_input_codes(h32, fmt: str, a2: float | None = None):
         return F.bf16_bits(h32), None
     if fmt == MXFP8:
         return F.mxfp8_quantize(h32)
+    if fmt == MXFP4:
+        return F.mxfp4_quantize(h32)
     return F.nvfp4_quantize(h32, np.float32(a2))
 
 

@@ -244,3 +244,77 @@ def test_nvfp4_zero_token():
     assert gs.tolist() == [1.0]
     packed, sb = F.nvfp4_quantize(np.zeros((1, 16), np.float32), gs)
     assert not packed.any() and not sb.any()
+
+
+# ----------------------------------------------------------------------------- MXFP4 (E2M1 + UE8M0 per 1x32)
+
+def test_mxfp4_golden_block(golden_dir):
+    g = _load(golden_dir, "mxfp4_block.json")
+    packed, sf = F.mxfp4_quantize(np.array([g["x"]]))
+    assert sf.tolist() == [[g["scale_byte"]]]
+    assert packed[0].tolist() == g["packed"]
+
+
+def test_mxfp4_exponent_exact_powers():
+    """amax = 6 * 2^n gives e = n; one ulp above gives n + 1."""
+    for n in (-20, -3, -1, 0, 1, 5, 30):
+        a = np.ldexp(6.0, n)
+        assert int(F.mx_exponent(a, 6.0)) == n
+        assert int(F.mx_exponent(np.nextafter(a, np.inf), 6.0)) == n + 1
+        assert int(F.mx_exponent(np.nextafter(a, 0.0), 6.0)) == n
+
+
+def test_mxfp4_round_trip_of_exact_grid():
+    """A block of E2M1 values times 2^e whose largest magnitude is 6 * 2^e quantises to
+    exactly those codes and scale byte e + 127."""
+    rng = np.random.default_rng(7)
+    for e in (-10, -1, 0, 3, 12):
+        codes = rng.integers(0, 16, size=(4, 32)).astype(np.uint8)
+        codes[:, 5] = 7 | (rng.integers(0, 2, size=4) << 3).astype(np.uint8)   # +-6: fixes the exponent
+        x = F.E2M1_TABLE[codes] * np.ldexp(1.0, e)
+        packed, sf = F.mxfp4_quantize(x)
+        assert np.array_equal(sf, np.full((4, 1), e + 127, np.uint8))
+        got = F.unpack_e2m1(packed)
+        # +0 and -0 both decode to 0; compare values, then signs of the non-zeros
+        assert np.array_equal(F.E2M1_TABLE[got], F.E2M1_TABLE[codes])
+
+
+def test_mxfp4_brute_force_nearest():
+    """Codes against an exhaustive nearest-value search over the 8 magnitudes (ties to the
+    even code), block by block, on random data including exact midpoints."""
+    rng = np.random.default_rng(11)
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    x = rng.normal(size=(64, 32)) * np.exp2(rng.integers(-4, 5, size=(64, 1)))
+    x[::7, 3] = np.ldexp(1.25, 2)      # midpoints show up at some scales
+    packed, sf = F.mxfp4_quantize(x)
+    codes = F.unpack_e2m1(packed)
+    for r in range(x.shape[0]):
+        e = int(sf[r, 0]) - 127
+        assert np.abs(x[r]).max() <= 6.0 * 2.0 ** e and (e == -127 or np.abs(x[r]).max() > 3.0 * 2.0 ** e)
+        for i in range(32):
+            v = abs(x[r, i]) / 2.0 ** e
+            d = np.abs(mags - v)
+            best = np.flatnonzero(d == d.min())
+            want = best[0] if len(best) == 1 else next(b for b in best if b % 2 == 0)
+            assert codes[r, i] & 7 == want, (r, i, v)
+            if codes[r, i] & 7:
+                assert (codes[r, i] >> 3) == (x[r, i] < 0)
+
+
+def test_mxfp4_error_bound():
+    """|x - dequant(quant(x))| <= half the largest E2M1 gap (1) times the block scale, and
+    <= a quarter of the scale where |x| <= the scale (gap 0.5 there)."""
+    rng = np.random.default_rng(3)
+    x = rng.normal(size=(128, 64)) * 3.0
+    packed, sf = F.mxfp4_quantize(x)
+    d = F.mxfp4_dequantize(packed, sf)
+    scale = np.repeat(np.ldexp(1.0, sf.astype(np.int64) - 127), 32, axis=1)
+    err = np.abs(x - d)
+    assert np.all(err <= scale * (1 + 1e-12))
+    small = np.abs(x) <= scale
+    assert np.all(err[small] <= 0.25 * scale[small] * (1 + 1e-12))
+
+
+def test_mxfp4_zero_block():
+    packed, sf = F.mxfp4_quantize(np.zeros((2, 32)))
+    assert np.all(packed == 0) and np.all(sf == 127)
