@@ -37,9 +37,9 @@ DEFAULT_WORKLOAD = "mxfp8_small"
 FLUSH_BYTES = 256 << 20
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dense tensor throughput relative to bf16 (nominal 2.25 / 4.5 / 13.5 PFLOP/s)
-TENSOR_RATIO = {"bf16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0}
-ELEM_BYTES = {"bf16": 2.0, "mxfp8": 1.0, "nvfp4": 0.5}
-SF_PER_ELEM = {"bf16": 0.0, "mxfp8": 1.0 / 32, "nvfp4": 1.0 / 16}
+TENSOR_RATIO = {"bf16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0, "mxfp4": 6.0}
+ELEM_BYTES = {"bf16": 2.0, "mxfp8": 1.0, "nvfp4": 0.5, "mxfp4": 0.5}
+SF_PER_ELEM = {"bf16": 0.0, "mxfp8": 1.0 / 32, "nvfp4": 1.0 / 16, "mxfp4": 1.0 / 32}
 # DRAM bytes (read + write) per launch from one ncu capture of the current kernels
 # (profiles/grouped_gemm_*.md); an entry must be removed when its kernel changes. The
 # nvfp4_decode entries come from a capture at E=64 scaled by touched experts (249 / 64).
@@ -50,7 +50,7 @@ NCU_TRAFFIC = {
 }
 # tokens of one reference-arm step, and of the first (sizing) call of cpu_baseline
 CPU_SAMPLE_TOKENS = {"bf16_toy": 64, "mxfp8_small": 24, "nvfp4_decode": 3, "mxfp8_prefill_zipf": 12,
-                     "nvfp4_shared_norm": 6}
+                     "nvfp4_shared_norm": 6, "mxfp4_small": 24}
 
 
 # ----------------------------------------------------------------------------- distributed plumbing
@@ -238,12 +238,13 @@ def oracle_baseline(shape: S.MoeShape, target_s: float = 12.0):
     seconds of host work. When even the whole batch takes less, the whole batch is run repeatedly until
     target_s has passed. Returns (seconds, tokens, cores, description)."""
     smp = OracleSample(shape)
-    n0 = min(CPU_SAMPLE_TOKENS[shape.name.split("+")[0]], shape.T)
-    dt0 = smp.time(n0)
-    n1 = max(n0, min(shape.T, int(n0 * target_s / max(dt0, 1e-3))))
-    dt = smp.time(n1) if n1 != n0 else dt0
-    if n1 < shape.T or dt >= target_s:
-        return dt, n1, blas_threads(), f"first {n1} tokens of {shape.name}"
+    n = min(CPU_SAMPLE_TOKENS[shape.name.split("+")[0]], shape.T)
+    dt = smp.time(n)
+    while dt < target_s and n < shape.T:   # the oracle's time grows slower than its token count
+        n = min(shape.T, max(n + 1, int(n * target_s / max(dt, 1e-3))))
+        dt = smp.time(n)
+    if dt >= target_s or n < shape.T:
+        return dt, n, blas_threads(), f"first {n} tokens of {shape.name}"
     total, reps = dt, 1
     while total < target_s:
         total += smp.time(shape.T)

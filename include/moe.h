@@ -52,6 +52,7 @@ extern "C" {
 #define MOE_FMT_BF16   0
 #define MOE_FMT_MXFP8  1
 #define MOE_FMT_NVFP4  2
+#define MOE_FMT_MXFP4  3   /* E2M1 codes, one UE8M0 scale per 1x32 block (weights, dispatch, L2 input) */
 
 #define MOE_ACT_SWIGLU 0
 

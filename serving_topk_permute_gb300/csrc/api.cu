@@ -34,7 +34,8 @@ Dims dims_of(const moe_config_t& c) {
 
 int validate(const moe_config_t* c) {
     if (!c) return MOE_ERR_INVALID_ARG;
-    if (c->format != MOE_FMT_BF16 && c->format != MOE_FMT_MXFP8 && c->format != MOE_FMT_NVFP4)
+    if (c->format != MOE_FMT_BF16 && c->format != MOE_FMT_MXFP8 && c->format != MOE_FMT_NVFP4 &&
+        c->format != MOE_FMT_MXFP4)
         return MOE_ERR_UNSUPPORTED;
     if (c->activation != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
     if (c->num_experts < 1 || c->num_experts > MAX_EXPERTS) return MOE_ERR_INVALID_ARG;
@@ -42,7 +43,8 @@ int validate(const moe_config_t* c) {
     if (c->max_tokens < 1) return MOE_ERR_INVALID_ARG;
     if (c->hidden < 128 || c->inter < 128 || c->hidden % 128 || c->inter % 128) return MOE_ERR_INVALID_ARG;
     if (c->hidden > MAX_HIDDEN) return MOE_ERR_INVALID_ARG;
-    if (c->format == MOE_FMT_NVFP4 && (c->hidden % 256 || c->inter % 256)) return MOE_ERR_INVALID_ARG;
+    if ((c->format == MOE_FMT_NVFP4 || c->format == MOE_FMT_MXFP4) && (c->hidden % 256 || c->inter % 256))
+        return MOE_ERR_INVALID_ARG;  // a 128-byte K stage holds 256 four-bit elements
     if (!isfinite(c->act_alpha) || !isfinite(c->act_beta)) return MOE_ERR_INVALID_ARG;
     if (c->act_has_clamp && !(c->act_clamp >= 0.0f)) return MOE_ERR_INVALID_ARG;
     if (c->shared_inter < 0 || c->shared_inter % 128) return MOE_ERR_INVALID_ARG;
@@ -245,7 +247,7 @@ int moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     if (!get_encode()) return MOE_ERR_CUDA;
     CUDA_TRY(route_prepare(MAX_EXPERTS));
-    for (int f = MOE_FMT_BF16; f <= MOE_FMT_NVFP4; ++f) {
+    for (int f = MOE_FMT_BF16; f <= MOE_FMT_MXFP4; ++f) {
         CUDA_TRY(gemm_prepare(f));
         CUDA_TRY(gemm2_prepare(f));
         CUDA_TRY(fused_prepare(f));

@@ -29,10 +29,14 @@ constexpr unsigned long long DRAIN_TIMEOUT_NS = 2000000000ull;
 
 // per-format constants
 __host__ __device__ constexpr int fmt_elem_bits(int fmt) { return fmt == MOE_FMT_BF16 ? 16 : (fmt == MOE_FMT_MXFP8 ? 8 : 4); }
-// scale-factor atoms per K stage (each atom covers 4 scale blocks along K)
-__host__ __device__ constexpr int fmt_sf_atoms(int fmt) { return fmt == MOE_FMT_BF16 ? 0 : (fmt == MOE_FMT_MXFP8 ? 1 : 4); }
+// scale-factor atoms per K stage (each atom covers 4 scale blocks along K): a 128-byte
+// stage holds 128 MXFP8 (4 blocks of 32), 256 NVFP4 (16 blocks of 16) or 256 MXFP4
+// (8 blocks of 32) elements
+__host__ __device__ constexpr int fmt_sf_atoms(int fmt) {
+    return fmt == MOE_FMT_BF16 ? 0 : (fmt == MOE_FMT_MXFP8 ? 1 : (fmt == MOE_FMT_MXFP4 ? 2 : 4));
+}
 // elements per scale block
-__host__ __device__ constexpr int fmt_sf_block(int fmt) { return fmt == MOE_FMT_MXFP8 ? 32 : 16; }
+__host__ __device__ constexpr int fmt_sf_block(int fmt) { return fmt == MOE_FMT_NVFP4 ? 16 : 32; }
 // bytes of one row of K elements
 __host__ __device__ inline int64_t fmt_row_bytes(int fmt, int64_t K) { return K * fmt_elem_bits(fmt) / 8; }
 // number of 128-byte K stages for K elements
@@ -326,6 +330,17 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
     asm volatile(
@@ -349,6 +364,13 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(int n, uint32_t sf_id) {
 // kind::mxf4nvf4: A/B E2M1 (1), scale type UE4M3 (bit 23 = 0).
 __host__ __device__ constexpr uint32_t idesc_nvf4(int n) {
     return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+// kind::mxf4nvf4 with scale_vec::2X (MXFP4): A/B E2M1, scale type UE8M0 (bit 23); each
+// MMA (K = 64) takes two scales per row, bytes sf_id and sf_id + 1 (sf_id 0 or 2) of
+// the row's 32-bit scale column.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int n, uint32_t sf_id) {
+    return (sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
 }
 
 // load 32 consecutive fp32 columns of this warp's 32 lanes (one row per thread)
@@ -488,6 +510,16 @@ __device__ __forceinline__ void mma2_mxf8(uint32_t d_tmem, uint64_t adesc, uint6
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
+__device__ __forceinline__ void mma2_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void mma2_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
     asm volatile(
@@ -535,6 +567,15 @@ __device__ __forceinline__ int ue8m0_exponent(float amax) {
     int p;
     const float f = frexpf(amax, &p);
     int e = (f <= 0.875f) ? p - 9 : p - 8;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+// MXFP4 block exponent: the smallest e with amax <= 6 * 2^e. With amax = f * 2^p,
+// f in [0.5, 1): 6 * 2^(p-3) = 0.75 * 2^p, so e = p - 3 when f <= 0.75, else p - 2.
+__device__ __forceinline__ int ue8m0_exponent_fp4(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    int p;
+    const float f = frexpf(amax, &p);
+    int e = (f <= 0.75f) ? p - 3 : p - 2;
     return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 

@@ -173,6 +173,26 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 3)
                     const int r = s_rows[j];
                     if (r >= 0) reinterpret_cast<uint4*>(a.xq + (int64_t)r * a.H * 2)[c] = v[i];
                 }
+        } else if (a.fmt == MOE_FMT_MXFP4) {
+            // a 1x32 block is 4 neighbouring threads: exponent from the block amax, then
+            // E2M1 codes of x * 2^-e, 8 codes (4 bytes) per thread
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const int ex = ue8m0_exponent_fp4(amax);
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                word |= cvt_e2m1x2(ldexpf(f[2 * j], -ex), ldexpf(f[2 * j + 1], -ex)) << (8 * j);
+            if (in)
+                for (int j = 0; j < k; ++j) {
+                    const int r = s_rows[j];
+                    if (r < 0) continue;
+                    reinterpret_cast<uint32_t*>(a.xq + (int64_t)r * (a.H / 2))[c] = word;
+                    if ((c & 3) == 0) a.xsf[act_sf_offset(r, c / 4, 2, nks_x)] = (uint8_t)(ex + 127);
+                }
         } else if (a.fmt == MOE_FMT_MXFP8) {
             const int ex = mxfp8_block_exponent(f);
             const uint2 codes = mxfp8_chunk(f, ex);

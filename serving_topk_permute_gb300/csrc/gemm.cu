@@ -189,6 +189,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const uint32_t accumulate = (ks > 0 || j > 0) ? 1u : 0u;
                         if constexpr (FMT == MOE_FMT_BF16)
                             mma_bf16(d_tmem, ad, bd, idesc_bf16(BN), accumulate);
+                        else if constexpr (FMT == MOE_FMT_MXFP4)
+                            mma_mxf4(d_tmem, ad, bd, idesc_mxf4(BN, 2u * (j & 1)), sfa_col + 4 * (j >> 1),
+                                     sfb_col + 4 * NB * (j >> 1), accumulate);
                         else if constexpr (FMT == MOE_FMT_MXFP8)
                             mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BN, j), sfa_col, sfb_col, accumulate);
                         else
@@ -272,6 +275,7 @@ cudaError_t gemm_prepare(int fmt) {
     switch (fmt) {
         case MOE_FMT_BF16: return prepare_fmt<MOE_FMT_BF16>();
         case MOE_FMT_MXFP8: return prepare_fmt<MOE_FMT_MXFP8>();
+        case MOE_FMT_MXFP4: return prepare_fmt<MOE_FMT_MXFP4>();
         default: return prepare_fmt<MOE_FMT_NVFP4>();
     }
 }
@@ -300,6 +304,7 @@ cudaError_t launch_gemm(int fmt, bool l1, int bn, const CUtensorMap& tmA, const 
     switch (fmt) {
         case MOE_FMT_BF16: return launch_fmt<MOE_FMT_BF16>(l1, bn, tmA, tmB, a, grid, st, pdl);
         case MOE_FMT_MXFP8: return launch_fmt<MOE_FMT_MXFP8>(l1, bn, tmA, tmB, a, grid, st, pdl);
+        case MOE_FMT_MXFP4: return launch_fmt<MOE_FMT_MXFP4>(l1, bn, tmA, tmB, a, grid, st, pdl);
         default: return launch_fmt<MOE_FMT_NVFP4>(l1, bn, tmA, tmB, a, grid, st, pdl);
     }
 }

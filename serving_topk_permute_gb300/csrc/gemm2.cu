@@ -25,7 +25,7 @@ struct Gemm2Cfg {
     static constexpr int S = fmt_sf_atoms(FMT);
     static constexpr int BN = 256;                      // weight rows per pair tile
     static constexpr int NB = BN / NBLK;
-    static constexpr int STAGES = FMT == MOE_FMT_NVFP4 ? 5 : 6;
+    static constexpr int STAGES = FMT == MOE_FMT_NVFP4 ? 5 : 6;  // NVFP4's larger scale atoms leave room for 5
     static constexpr int A_BYTES = BM * BK_BYTES;      // this CTA's 128 rows
     static constexpr int B_BYTES = NBLK * BK_BYTES;    // this CTA's half of the weight rows
     static constexpr int SFA_BYTES = S * ATOM_BYTES;
@@ -212,6 +212,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const uint32_t accumulate = (ks > 0 || j > 0) ? 1u : 0u;
                         if constexpr (FMT == MOE_FMT_BF16)
                             mma2_bf16(tmem_base, ad, bd, idesc_m(idesc_bf16(BN), 2 * BM), accumulate);
+                        else if constexpr (FMT == MOE_FMT_MXFP4)
+                            mma2_mxf4(tmem_base, ad, bd, idesc_m(idesc_mxf4(BN, 2u * (j & 1)), 2 * BM),
+                                      sfa_col + 4 * (j >> 1), sfb_col + 4 * NB * (j >> 1), accumulate);
                         else if constexpr (FMT == MOE_FMT_MXFP8)
                             mma2_mxf8(tmem_base, ad, bd, idesc_m(idesc_mxf8(BN, j), 2 * BM), sfa_col, sfb_col,
                                       accumulate);
@@ -294,6 +297,9 @@ cudaError_t gemm2_prepare(int fmt) {
         case MOE_FMT_MXFP8:
             if ((e = set_attr2<MOE_FMT_MXFP8, true>()) != cudaSuccess) return e;
             return set_attr2<MOE_FMT_MXFP8, false>();
+        case MOE_FMT_MXFP4:
+            if ((e = set_attr2<MOE_FMT_MXFP4, true>()) != cudaSuccess) return e;
+            return set_attr2<MOE_FMT_MXFP4, false>();
         default:
             if ((e = set_attr2<MOE_FMT_NVFP4, true>()) != cudaSuccess) return e;
             return set_attr2<MOE_FMT_NVFP4, false>();
@@ -319,6 +325,9 @@ cudaError_t launch_gemm2(int fmt, bool l1, const CUtensorMap& tmA, const CUtenso
         case MOE_FMT_MXFP8:
             return l1 ? launch2_t<MOE_FMT_MXFP8, true>(tmA, tmB, tmSFA, tmSFB, a, grid, st, pdl)
                       : launch2_t<MOE_FMT_MXFP8, false>(tmA, tmB, tmSFA, tmSFB, a, grid, st, pdl);
+        case MOE_FMT_MXFP4:
+            return l1 ? launch2_t<MOE_FMT_MXFP4, true>(tmA, tmB, tmSFA, tmSFB, a, grid, st, pdl)
+                      : launch2_t<MOE_FMT_MXFP4, false>(tmA, tmB, tmSFA, tmSFB, a, grid, st, pdl);
         default:
             return l1 ? launch2_t<MOE_FMT_NVFP4, true>(tmA, tmB, tmSFA, tmSFB, a, grid, st, pdl)
                       : launch2_t<MOE_FMT_NVFP4, false>(tmA, tmB, tmSFA, tmSFB, a, grid, st, pdl);

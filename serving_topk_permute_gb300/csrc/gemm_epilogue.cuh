@@ -101,6 +101,23 @@ __device__ __forceinline__ void epilogue_l1(const GemmArgs& p, uint32_t tacc, in
         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
         dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
         p.hsf[act_sf_offset(row, hc / 32, 1, p.h_nks)] = (uint8_t)(ex + 127);
+    } else if constexpr (FMT == MOE_FMT_MXFP4) {
+        // one 1x32 block: UE8M0 exponent with amax <= 6 * 2^ex, E2M1 codes of h * 2^-ex
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+        const int ex = ue8m0_exponent_fp4(amax);
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                word |= cvt_e2m1x2(ldexpf(h[8 * i + 2 * j], -ex), ldexpf(h[8 * i + 2 * j + 1], -ex)) << (8 * j);
+            w[i] = word;
+        }
+        *reinterpret_cast<uint4*>(p.hq + ((int64_t)row * p.I + hc) / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+        p.hsf[act_sf_offset(row, hc / 32, 2, p.h_nks)] = (uint8_t)(ex + 127);
     } else {
         const float denom = __fmul_rn(a2, 6.0f);
         uint32_t w[4];

@@ -264,6 +264,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const uint32_t accumulate = (ks > 0 || j > 0) ? 1u : 0u;
                         if constexpr (FMT == MOE_FMT_BF16)
                             mma_bf16(tmem_base, ad, bd, idesc_bf16(BN), accumulate);
+                        else if constexpr (FMT == MOE_FMT_MXFP4)
+                            mma_mxf4(tmem_base, ad, bd, idesc_mxf4(BN, 2u * (j & 1)), sfa_col + 4 * (j >> 1),
+                                     sfb_col + 4 * NB * (j >> 1), accumulate);
                         else if constexpr (FMT == MOE_FMT_MXFP8)
                             mma_mxf8(tmem_base, ad, bd, idesc_mxf8(BN, j), sfa_col, sfb_col, accumulate);
                         else
@@ -347,6 +350,7 @@ cudaError_t fused_prepare(int fmt) {
     switch (fmt) {
         case MOE_FMT_BF16: return fused_attr<MOE_FMT_BF16>();
         case MOE_FMT_MXFP8: return fused_attr<MOE_FMT_MXFP8>();
+        case MOE_FMT_MXFP4: return fused_attr<MOE_FMT_MXFP4>();
         default: return fused_attr<MOE_FMT_NVFP4>();
     }
 }
@@ -366,6 +370,7 @@ cudaError_t launch_fused_mlp(int fmt, const CUtensorMap& a1, const CUtensorMap& 
     switch (fmt) {
         case MOE_FMT_BF16: return fused_t<MOE_FMT_BF16>(a1, b1, a2, b2, p1, p2, fs, grid, st, pdl);
         case MOE_FMT_MXFP8: return fused_t<MOE_FMT_MXFP8>(a1, b1, a2, b2, p1, p2, fs, grid, st, pdl);
+        case MOE_FMT_MXFP4: return fused_t<MOE_FMT_MXFP4>(a1, b1, a2, b2, p1, p2, fs, grid, st, pdl);
         default: return fused_t<MOE_FMT_NVFP4>(a1, b1, a2, b2, p1, p2, fs, grid, st, pdl);
     }
 }

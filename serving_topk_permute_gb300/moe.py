@@ -16,7 +16,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "lib
 _lib = None
 
 MOE_OK = 0
-FORMATS = {"bf16": 0, "mxfp8": 1, "nvfp4": 2}
+FORMATS = {"bf16": 0, "mxfp8": 1, "nvfp4": 2, "mxfp4": 3}
 
 # weight tensor ids (moe_weight_layout_size)
 W13, W13_SF, W2, W2_SF, SHARED_W13, SHARED_W13_SF, SHARED_W2, SHARED_W2_SF, W13_GS, W2_GS = range(10)

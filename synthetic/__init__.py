@@ -39,6 +39,7 @@ import numpy as np
 FMT_BF16 = "bf16"
 FMT_MXFP8 = "mxfp8"
 FMT_NVFP4 = "nvfp4"
+FMT_MXFP4 = "mxfp4"
 
 # stream ids (fixed draw order: one independent stream per tensor)
 _S_X, _S_LOGITS, _S_W13, _S_W2, _S_WS13, _S_WS2, _S_GAMMA, _S_A2, _S_SF13, _S_SF2, \
@@ -74,6 +75,8 @@ WORKLOADS = {
     "nvfp4_shared_norm": MoeShape("nvfp4_shared_norm", 4096, 4096, 1536, 128, 8,
                                   FMT_NVFP4, shared_I=4096, shared_fmt=FMT_MXFP8,
                                   post_norm=True),
+    # the MXFP8 layer's shape in MXFP4 (the format the pages also list for routed experts)
+    "mxfp4_small": MoeShape("mxfp4_small", 512, 2048, 768, 64, 8, FMT_MXFP4),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
@@ -172,6 +175,16 @@ def mxfp8_codes(rows: int, K: int, seed: int, stream: int, index: int = 0):
     return codes, sf
 
 
+def mxfp4_codes(rows: int, K: int, seed: int, stream: int, index: int = 0):
+    """Packed E2M1 bytes [rows, K/2] (every nibble equally likely, rms value 2.93) and
+    UE8M0 bytes [rows, K/32] around 1 / (2.93 sqrt(K)): weights of rms about 1/sqrt(K)."""
+    g = _rng(seed, stream, index)
+    codes = g.integers(0, 256, size=(rows, K // 2), dtype=np.uint16).astype(np.uint8)
+    centre = 127 + int(round(-math.log2(2.93) - 0.5 * math.log2(K)))
+    sf = g.integers(centre - 1, centre + 2, size=(rows, K // 32), dtype=np.int64).astype(np.uint8)
+    return codes, sf
+
+
 def nvfp4_codes(rows: int, K: int, seed: int, stream: int, index: int = 0):
     """Packed E2M1 bytes [rows, K/2], E4M3 block-scale bytes [rows, K/16], fp32 global scale."""
     g = _rng(seed, stream, index)
@@ -227,6 +240,15 @@ def routed_code_checkpoint(shape: MoeShape, seed: int = 0, experts=None) -> Chec
             w13[e], w13_sf[e] = mxfp8_codes(2 * I, H, seed, _S_W13, e)
             w2[e], w2_sf[e] = mxfp8_codes(H, I, seed, _S_W2, e)
         return Checkpoint(FMT_MXFP8, w13, w2, w13_sf, w2_sf)
+    if shape.fmt == FMT_MXFP4:
+        w13 = np.zeros((E, 2 * I, H // 2), np.uint8)
+        w13_sf = np.full((E, 2 * I, H // 32), 127, np.uint8)
+        w2 = np.zeros((E, H, I // 2), np.uint8)
+        w2_sf = np.full((E, H, I // 32), 127, np.uint8)
+        for e in sel:
+            w13[e], w13_sf[e] = mxfp4_codes(2 * I, H, seed, _S_W13, e)
+            w2[e], w2_sf[e] = mxfp4_codes(H, I, seed, _S_W2, e)
+        return Checkpoint(FMT_MXFP4, w13, w2, w13_sf, w2_sf)
     assert shape.fmt == FMT_NVFP4
     w13 = np.zeros((E, 2 * I, H // 2), np.uint8)
     w13_sf = np.zeros((E, 2 * I, H // 16), np.uint8)
@@ -283,6 +305,10 @@ def torch_code_checkpoint(shape: MoeShape, seed: int, device, shared: bool = Fal
         elif fmt == FMT_MXFP8:
             centre = 127 + int(round(-math.log2(96.0) - 0.5 * math.log2(K)))
             out[key] = ri(0x30, 0x7F, (E, rows, K)) | (ri(0, 2, (E, rows, K)) << 7)
+            out[key + "_sf"] = ri(centre - 1, centre + 2, (E, rows, K // 32))
+        elif fmt == FMT_MXFP4:
+            centre = 127 + int(round(-math.log2(2.93) - 0.5 * math.log2(K)))
+            out[key] = ri(0, 256, (E, rows, K // 2))
             out[key + "_sf"] = ri(centre - 1, centre + 2, (E, rows, K // 32))
         else:
             out[key] = ri(0, 256, (E, rows, K // 2))

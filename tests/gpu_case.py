@@ -21,7 +21,7 @@ from oracle import moe as OM
 import serving_topk_permute_gb300 as pkg
 
 # max |gpu - oracle| <= REL * rms(oracle) + ABS
-REL = {"bf16": 2e-2, "mxfp8": 2e-2, "nvfp4": 5e-2}
+REL = {"bf16": 2e-2, "mxfp8": 2e-2, "nvfp4": 5e-2, "mxfp4": 5e-2}   # MXFP4: 4-bit elements like NVFP4
 ABS = 1e-3
 
 

@@ -31,7 +31,12 @@ REDUCED = {
     "nvfp4_decode": S.shrink(W["nvfp4_decode"], T=40, H=1024, I=512, E=32, k=8),
     "mxfp8_prefill_zipf": S.shrink(W["mxfp8_prefill_zipf"], T=512, H=768, I=256, E=32, k=8),
     "nvfp4_shared_norm": S.shrink(W["nvfp4_shared_norm"], T=130, H=512, I=256, E=16, k=4, shared_I=512),
+    "mxfp4_small": S.shrink(W["mxfp4_small"], T=200, H=512, I=512, E=16, k=4),
 }
+# bytes per element, scale atoms per 128-byte K stage, elements per scale block
+ROW_BYTES = {"mxfp8": 1.0, "nvfp4": 0.5, "mxfp4": 0.5}
+SF_ATOMS = {"mxfp8": 1, "nvfp4": 4, "mxfp4": 2}
+SF_BLOCK = {"mxfp8": 32, "nvfp4": 16, "mxfp4": 32}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -73,11 +78,11 @@ def test_routing_and_dispatch_bit_exact_full_size(name):
         got = xq.reshape(-1, shape.H * 2)[rows].view(np.uint16)
         assert np.array_equal(got, case.x[toks])
         return
-    row_bytes = shape.H if shape.fmt == "mxfp8" else shape.H // 2
+    row_bytes = int(shape.H * ROW_BYTES[shape.fmt])
     got_codes = xq.reshape(-1, row_bytes)[rows]
     assert np.array_equal(got_codes, d.codes[toks])
-    S_atoms = 1 if shape.fmt == "mxfp8" else 4
-    nblk = shape.H // (32 if shape.fmt == "mxfp8" else 16)
+    S_atoms = SF_ATOMS[shape.fmt]
+    nblk = shape.H // SF_BLOCK[shape.fmt]
     got_sf = G.unpack_act_sf(G.region_u8(run, T, "xsf"), rows, nblk, S_atoms)
     assert np.array_equal(got_sf, d.sf[toks])
     if shape.fmt == "nvfp4":
@@ -106,7 +111,7 @@ def _near_midpoint(v, a, b, tau):
     return np.abs(v - (a + b) / 2) <= tau
 
 
-@pytest.mark.parametrize("name", ["mxfp8_small", "nvfp4_decode", "nvfp4_shared_norm", "bf16_toy"])
+@pytest.mark.parametrize("name", ["mxfp8_small", "nvfp4_decode", "nvfp4_shared_norm", "bf16_toy", "mxfp4_small"])
 def test_l2_input_matches_oracle(name):
     """The GPU's fp32 h against the oracle's h, and the GPU's L2-input codes against the
     oracle's codes of its own h: equal except where the oracle's value sits within
@@ -138,9 +143,9 @@ def test_l2_input_matches_oracle(name):
         assert diff.mean() < 1e-3
         return
     fmt = shape.fmt
-    rb = I if fmt == "mxfp8" else I // 2
+    rb = int(I * ROW_BYTES[fmt])
     got_codes = hq.reshape(-1, rb)[rows]
-    S_atoms, g = (1, 32) if fmt == "mxfp8" else (4, 16)
+    S_atoms, g = SF_ATOMS[fmt], SF_BLOCK[fmt]
     got_sf = G.unpack_act_sf(G.region_u8(run, T, "hsf"), rows, I // g, S_atoms)
     # block scales: a differing scale byte needs the block's amax at a decision boundary
     amax = np.abs(h_or.astype(np.float32).astype(np.float64)).reshape(len(rows), -1, g).max(-1)
@@ -153,6 +158,15 @@ def test_l2_input_matches_oracle(name):
         deq_gpu = OF.mxfp8_dequantize(got_codes, got_sf)
         scale = OF.UE8M0_TABLE[sf].repeat(g, axis=1)
         step = scale * 2.0 ** (np.floor(np.log2(np.maximum(np.abs(h_or) / scale, 2.0 ** -6))) - 3)
+    elif fmt == "mxfp4":
+        e = sf[sf_diff].astype(np.int64) - 127
+        bound = np.ldexp(6.0, np.minimum(e, got_sf[sf_diff].astype(np.int64) - 127))
+        assert np.all(np.abs(amax[sf_diff] - bound) <= TAU)
+        deq_or = OF.mxfp4_dequantize(codes, sf)
+        deq_gpu = OF.mxfp4_dequantize(got_codes, got_sf)
+        scale = OF.UE8M0_TABLE[sf].repeat(g, axis=1)
+        q = np.abs(h_or) / scale
+        step = scale * np.where(q < 2, 0.5, np.where(q < 4, 1.0, 2.0))
     else:
         a2 = np.float32(case.layer.a2)
         ratio = amax / (float(a2) * 6.0)
@@ -175,7 +189,8 @@ def test_l2_input_matches_oracle(name):
 
 # ----------------------------------------------------------------------------- outputs, full size, sampled tokens
 
-@pytest.mark.parametrize("name", ["mxfp8_small", "nvfp4_decode", "mxfp8_prefill_zipf", "nvfp4_shared_norm"])
+@pytest.mark.parametrize("name", ["mxfp8_small", "nvfp4_decode", "mxfp8_prefill_zipf", "nvfp4_shared_norm",
+                                  "mxfp4_small"])
 def test_forward_matches_oracle_full_size_sampled(name):
     shape = W[name]
     T = shape.T
@@ -189,12 +204,12 @@ def test_forward_matches_oracle_full_size_sampled(name):
 # ----------------------------------------------------------------------------- edge cases
 
 def _small_case(fmt="mxfp8", **kw):
-    base = {"bf16": "bf16_toy", "mxfp8": "mxfp8_small", "nvfp4": "nvfp4_decode"}[fmt]
+    base = {"bf16": "bf16_toy", "mxfp8": "mxfp8_small", "nvfp4": "nvfp4_decode", "mxfp4": "mxfp4_small"}[fmt]
     shape = S.shrink(W[base], **{"T": 64, "H": 256, "I": 256, "E": 8, "k": 2, **kw})
     return shape
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4"])
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4", "mxfp4"])
 def test_single_token(fmt):
     shape = _small_case(fmt, T=1)
     case = G.float_case(shape)
@@ -333,12 +348,11 @@ def _expected_interleave(w13: np.ndarray, I: int) -> np.ndarray:
     return out
 
 
-def _expected_sf_atoms(sf: np.ndarray, N: int, K: int, g: int, interleave: bool, I: int) -> np.ndarray:
+def _expected_sf_atoms(sf: np.ndarray, N: int, K: int, g: int, interleave: bool, I: int, S_atoms: int) -> np.ndarray:
     """Row 32j+i / scale b of 4 at byte 16i + 4j + b of a 512-byte atom (the UTCCP row
     permutation 128c + 32j + i -> 128c + 4i + j in 32-bit words), atoms
     [E][K stage][128-row block][S], blocks = round_up(N, 256) / 128."""
     E = sf.shape[0]
-    S_atoms = 1 if g == 32 else 4
     nkb = K // g
     nks = nkb // (4 * S_atoms)
     nblk = -(-N // 256) * 2
@@ -355,7 +369,7 @@ def _expected_sf_atoms(sf: np.ndarray, N: int, K: int, g: int, interleave: bool,
     return out.reshape(-1)
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4"])
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4", "mxfp4"])
 def test_weight_transform_layout(fmt):
     shape = _small_case(fmt, H=512 if fmt != "mxfp8" else 384, I=256, E=3)
     case = G.float_case(shape)
@@ -367,9 +381,9 @@ def test_weight_transform_layout(fmt):
     assert np.array_equal(kw["w2"], ew.w2.view(np.uint8).reshape(-1))
     if fmt == "bf16":
         return
-    g = 32 if fmt == "mxfp8" else 16
-    assert np.array_equal(kw["w13_sf"], _expected_sf_atoms(ew.w13_sf, 2 * shape.I, shape.H, g, True, shape.I))
-    assert np.array_equal(kw["w2_sf"], _expected_sf_atoms(ew.w2_sf, shape.H, shape.I, g, False, shape.I))
+    g = SF_BLOCK[fmt]
+    assert np.array_equal(kw["w13_sf"], _expected_sf_atoms(ew.w13_sf, 2 * shape.I, shape.H, g, True, shape.I, SF_ATOMS[fmt]))
+    assert np.array_equal(kw["w2_sf"], _expected_sf_atoms(ew.w2_sf, shape.H, shape.I, g, False, shape.I, SF_ATOMS[fmt]))
     if fmt == "nvfp4":
         assert np.array_equal(kw["w13_gs"], ew.w13_gs) and np.array_equal(kw["w2_gs"], ew.w2_gs)
 
