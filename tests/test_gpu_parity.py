@@ -32,6 +32,9 @@ REDUCED = {
     "mxfp8_prefill_zipf": S.shrink(W["mxfp8_prefill_zipf"], T=512, H=768, I=256, E=32, k=8),
     "nvfp4_shared_norm": S.shrink(W["nvfp4_shared_norm"], T=130, H=512, I=256, E=16, k=4, shared_I=512),
     "mxfp4_small": S.shrink(W["mxfp4_small"], T=200, H=512, I=512, E=16, k=4),
+    # NVFP4 routed experts beside a BF16 shared expert (the other shared precision the pages list)
+    "nvfp4_bf16_shared": S.shrink(W["nvfp4_shared_norm"], name="nvfp4_bf16_shared", T=130, H=512, I=256, E=16, k=4,
+                                  shared_I=512, shared_fmt="bf16"),
 }
 # bytes per element, scale atoms per 128-byte K stage, elements per scale block
 ROW_BYTES = {"mxfp8": 1.0, "nvfp4": 0.5, "mxfp4": 0.5}
