@@ -243,6 +243,21 @@ def test_all_tokens_one_expert(fmt, mode):
     assert off.tolist() == [0, 0, 0, 0, 0, 0, pad, pad, pad]
 
 
+@pytest.mark.parametrize("E,k,T", [(512, 8, 300), (64, 32, 70), (40, 6, 333), (7, 5, 97)])
+def test_routing_limits_and_ragged_chunks(E, k, T):
+    """The largest expert count and top-k, and k that does not divide the routing chunk (a
+    token's slots straddle two chunks): routing bit-exact, outputs within tolerance."""
+    shape = _small_case("mxfp8", T=T, E=E, k=k, I=128)
+    case = G.float_case(shape)
+    run = G.run_gpu(case)
+    cnt, off, src, inv = OR.permute(case.ids, E, run.plan.block_m(T))
+    assert np.array_equal(G.region_i32(run, T, "counts")[:E], cnt)
+    assert np.array_equal(G.region_i32(run, T, "offsets")[:E + 1], off)
+    assert np.array_equal(G.region_i32(run, T, "src")[:int(off[-1])], src)
+    assert np.array_equal(G.region_i32(run, T, "inv_perm")[:T * k].reshape(T, k), inv)
+    G.assert_close(G.out_f64(run), G.oracle_out(case), "mxfp8", f"E={E} k={k}")
+
+
 def test_bad_expert_id_reports_status_and_is_masked():
     shape = _small_case("bf16", T=32)
     ids, w = S.router(shape)
