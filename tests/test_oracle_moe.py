@@ -189,3 +189,24 @@ def test_shared_expert_and_norm_compose():
     zn = F.bf16_bits_to_f64(M.forward(layer, x, ids, w))
     # rms of a normalised row is 1 (up to bf16 rounding)
     assert np.allclose(np.sqrt(np.mean(zn ** 2, axis=1)), 1.0, atol=4e-3)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4", "mxfp4"])
+def test_batched_layout_equals_routed_top1(fmt):
+    """The batched (masked) layout is the routed layer with top_k = 1 and weight 1: every
+    token goes to one expert, and its slot's row of the routed output is its batched row."""
+    shape, layer, _, _, _ = _small(fmt, T=24, E=4, k=1)
+    cap = 8
+    counts = np.array([3, 0, 8, 5])
+    xb = S.hidden_states(S.shrink(shape, T=4 * cap)).reshape(4, cap, shape.H)
+    out_b = M.forward_batched(layer, xb, counts)
+    # the same rows as a routed batch: token i of expert e -> expert e, weight 1
+    rows = [(e, m) for e in range(4) for m in range(counts[e])]
+    x_r = np.stack([xb[e, m] for e, m in rows])
+    ids = np.array([[e] for e, _ in rows])
+    w = np.ones((len(rows), 1), np.float32)
+    out_r = M.forward(layer, x_r, ids, w)
+    for i, (e, m) in enumerate(rows):
+        assert np.array_equal(out_b[e, m], out_r[i]), (e, m)
+    for e in range(4):
+        assert not out_b[e, counts[e]:].any()
