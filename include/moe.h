@@ -231,6 +231,27 @@ int moe_forward(moe_plan_t plan, int32_t num_tokens,
                 void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The routed experts on the batched (masked) layout (vllm.model_executor.layers.fused_moe,
+ * BatchedDeepGemmExperts.apply: m-grouped GEMMs over [E, max_num_tokens, K] with
+ * expert_num_tokens[E], then the activation with requantisation, then the second GEMM).
+ *   hidden            bf16 [E, max_tokens, H]: expert e's rows in its own slab
+ *   expert_num_tokens int32 [E] (device): the first expert_num_tokens[e] rows of slab e are used
+ *   out               bf16 [E, max_tokens, H]: rows m < expert_num_tokens[e] are written, the
+ *                     others are left as they are
+ * Each used row is quantised in the plan's format (its own NVFP4 scale), then goes through
+ * its expert's L1 -> activation -> L2 requantisation -> L2, exactly as a routed row with
+ * weight 1. No routing, no combine, no shared expert and no norm (the plan's are ignored).
+ * max_tokens: a multiple of 128 (each slab is whole row tiles). Needs the one-kernel GEMM
+ * (MOE_FLAG_CTA_PAIR, MOE_FLAG_TILE_128 and MOE_FLAG_SPLIT_GEMM return MOE_ERR_UNSUPPORTED).
+ * A count outside [0, max_tokens] is clamped and reported as MOE_ERR_CAPACITY by
+ * moe_last_status. Stream-ordered; workspace from moe_batched_workspace_size.
+ */
+int moe_batched_workspace_size(moe_plan_t plan, int32_t max_tokens, size_t* bytes);
+int moe_forward_batched(moe_plan_t plan, int32_t max_tokens, const void* hidden, const int32_t* expert_num_tokens,
+                        const moe_weights_t* weights, const float* l2_act_scale, void* out, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
  * Synchronise the stream and read (then clear) the device error word of the
  * workspace: *status = MOE_OK, MOE_ERR_BAD_EXPERT_ID or MOE_ERR_TIMEOUT.
  */

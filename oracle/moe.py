@@ -254,25 +254,25 @@ def forward(layer: Layer, x_bits, topk_ids, topk_weights, tokens=None, block_m: 
     return out
 
 
-def forward_batched(layer: Layer, x_bits, expert_num_tokens) -> np.ndarray:
+def forward_batched(layer: Layer, x_bits, expert_num_tokens, exact: bool = False) -> np.ndarray:
     """The routed experts on the batched (masked) layout (vllm.model_executor.layers.fused_moe,
     ``BatchedDeepGemmExperts.apply``): ``x_bits`` bf16 bits [E, M, H] holds each expert's rows
     in its own slab, of which the first ``expert_num_tokens[e]`` are used. Each used row is
     quantised on its own (the dispatch quantiser), then L1 -> activation -> L2 requant -> L2
-    of its expert. Returns bf16 bits [E, M, H] with the unused rows zero. No routing weights,
-    no combine, no shared expert, no norm.
+    of its expert. Returns bf16 bits [E, M, H] with the unused rows zero (``exact``: the fp64
+    values before that rounding). No routing weights, no combine, no shared expert, no norm.
     """
     x_bits = np.asarray(x_bits)
     E, M, H = x_bits.shape
     counts = np.asarray(expert_num_tokens, dtype=np.int64)
-    out = np.zeros((E, M, H), dtype=np.uint16)
+    out = np.zeros((E, M, H), dtype=np.float64 if exact else np.uint16)
     for e in range(E):
         n = int(counts[e])
         if n <= 0:
             continue
         d = dispatch_quantize(x_bits[e, :n], layer.routed.fmt)
         y = expert_mlp(d.x, layer.routed.w13_of(e), layer.routed.w2_of(e), layer.routed.fmt, layer.act, layer.a2)
-        out[e, :n] = F.bf16_bits(y)
+        out[e, :n] = y if exact else F.bf16_bits(y)
     return out
 
 

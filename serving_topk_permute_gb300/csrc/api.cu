@@ -407,6 +407,13 @@ static int choose_bn(const moe_config_t& c, int64_t rows_per_expert) {
     return 256;
 }
 
+// Batched layout: row-tile first rows and per-expert used-row counts (see BatchedDeepGemmExperts)
+struct BatchRows {
+    const int* tile_row;
+    const int* counts;
+    int rows_per_expert;
+};
+
 // one expert MLP pass; m_tiles_* count 128-row tiles on single CTAs, 256-row tiles on pairs.
 // With 256-wide single-CTA tiles (the default), L1 and L2 run as one kernel (sched:
 // its zeroed counters); otherwise as two.
@@ -415,7 +422,7 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool p
                    const moe_weights_t* w, const int* m_tiles_dev, int m_tiles_host, int64_t m_tiles_max,
                    const int* tile_expert, const int* src, int m_valid, const float* x_scale, const float* a2,
                    uint8_t* hq, uint8_t* hsf, float* h_debug, __nv_bfloat16* y, int* err, bool activation,
-                   uint32_t* sched, cudaStream_t st) {
+                   uint32_t* sched, cudaStream_t st, const BatchRows* br = nullptr) {
     const moe_config_t& c = p->cfg;
     const int S = fmt_sf_atoms(fmt);
     const int bn = pair ? 2 * BM : choose_bn(c, 0);
@@ -428,6 +435,11 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool p
     g.tile_expert = tile_expert;
     g.src = src;
     g.m_valid = m_valid;
+    if (br) {
+        g.tile_row = br->tile_row;
+        g.counts = br->counts;
+        g.rows_per_expert = br->rows_per_expert;
+    }
     g.top_k = c.top_k;
     g.err = err;
     g.timeout_ns = p->timeout_ns;
@@ -592,6 +604,110 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
         CUDA_TRY(launch_combine(ca, st, plan->pdl));
     }
     return MOE_OK;
+}
+
+// ------------------------------------------------------------------ batched (masked) layout
+namespace {
+enum BRegion { B_ERR, B_META, B_TILE_EXPERT, B_TILE_ROW, B_XQ, B_XSF, B_XSCALE, B_HQ, B_HSF, B_SCHED, B_COUNT };
+struct BLayout {
+    int64_t off[B_COUNT];
+    int64_t size[B_COUNT];
+    int64_t total, rows, tiles;
+};
+
+BLayout batched_layout_of(const moe_config_t& c, int M) {
+    BLayout L{};
+    const Dims d = dims_of(c);
+    L.rows = (int64_t)d.E * M;
+    L.tiles = L.rows / BM;
+    const int S = fmt_sf_atoms(d.fmt);
+    int64_t sz[B_COUNT] = {};
+    sz[B_ERR] = 16;  // first, at offset 0, as in moe_forward's workspace (moe_last_status reads it there)
+    sz[B_META] = 16;
+    sz[B_TILE_EXPERT] = 4 * L.tiles;
+    sz[B_TILE_ROW] = 4 * L.tiles;
+    sz[B_XQ] = L.rows * fmt_row_bytes(d.fmt, d.H);
+    sz[B_XSF] = L.tiles * fmt_k_stages(d.fmt, d.H) * S * ATOM_BYTES;
+    sz[B_XSCALE] = 4 * L.rows;
+    sz[B_HQ] = L.rows * fmt_row_bytes(d.fmt, d.I);
+    sz[B_HSF] = L.tiles * fmt_k_stages(d.fmt, d.I) * S * ATOM_BYTES;
+    sz[B_SCHED] = 4 * (1 + L.tiles);  // the GEMM's tile counter and done[tiles]
+    int64_t o = 0;
+    for (int r = 0; r < B_COUNT; ++r) {
+        L.off[r] = o;
+        L.size[r] = sz[r];
+        o += align_up(sz[r], REGION_ALIGN);
+    }
+    L.total = o;
+    return L;
+}
+
+int batched_check(const moe_config_t& c, int32_t M) {
+    if (M < BM || M % BM) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)c.num_experts * M >= ((int64_t)1 << 30)) return MOE_ERR_INVALID_ARG;  // int32 row indices
+    if (c.flags & (MOE_FLAG_CTA_PAIR | MOE_FLAG_TILE_128 | MOE_FLAG_SPLIT_GEMM)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+}  // namespace
+
+int moe_batched_workspace_size(moe_plan_t plan, int32_t max_tokens, size_t* bytes) {
+    if (!plan || !bytes) return MOE_ERR_INVALID_ARG;
+    const int v = batched_check(plan->cfg, max_tokens);
+    if (v != MOE_OK) return v;
+    *bytes = (size_t)batched_layout_of(plan->cfg, max_tokens).total;
+    return MOE_OK;
+}
+
+int moe_forward_batched(moe_plan_t plan, int32_t max_tokens, const void* hidden, const int32_t* expert_num_tokens,
+                        const moe_weights_t* weights, const float* l2_act_scale, void* out, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    const moe_config_t& c = plan->cfg;
+    const Dims d = dims_of(c);
+    const int v = batched_check(c, max_tokens);
+    if (v != MOE_OK) return v;
+    if (!hidden || !expert_num_tokens || !weights || !out || !workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned(hidden) || !aligned(expert_num_tokens) || !aligned(out) || !aligned(workspace))
+        return MOE_ERR_INVALID_ARG;
+    if (out == hidden) return MOE_ERR_INVALID_ARG;
+    if (!weights->w13 || !weights->w2) return MOE_ERR_INVALID_ARG;
+    if (d.fmt != MOE_FMT_BF16 && (!weights->w13_sf || !weights->w2_sf)) return MOE_ERR_INVALID_ARG;
+    if (d.fmt == MOE_FMT_NVFP4 && (!weights->w13_gs || !weights->w2_gs || !l2_act_scale)) return MOE_ERR_INVALID_ARG;
+    const BLayout L = batched_layout_of(c, max_tokens);
+    if (workspace_bytes < (size_t)L.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t* ws = (uint8_t*)workspace;
+    auto R = [&](int r) { return ws + L.off[r]; };
+    int* err = (int*)R(B_ERR);
+    int* meta = (int*)R(B_META);
+    uint32_t* sched = (uint32_t*)R(B_SCHED);
+    for (bool& r : plan->ran) r = false;
+    {
+        KernelTimer kt(plan, MOE_KERNEL_ROUTE, st);
+        CUDA_TRY(launch_batched_plan(expert_num_tokens, d.E, max_tokens, (int*)R(B_TILE_EXPERT), (int*)R(B_TILE_ROW),
+                                     meta, err, sched, (int)(1 + L.tiles), st, plan->pdl));
+    }
+    DispatchArgs da{};
+    da.x = (const uint16_t*)hidden;
+    da.T = (int)L.rows;
+    da.H = d.H;
+    da.k = 1;
+    da.E = d.E;
+    da.fmt = d.fmt;
+    da.xq = R(B_XQ);
+    da.xsf = R(B_XSF);
+    da.x_scale = (float*)R(B_XSCALE);
+    da.shared_fmt = -1;
+    da.batch_counts = expert_num_tokens;
+    da.batch_M = max_tokens;
+    {
+        KernelTimer kt(plan, MOE_KERNEL_DISPATCH, st);
+        CUDA_TRY(launch_dispatch(da, st, plan->pdl));
+    }
+    const BatchRows br{(const int*)R(B_TILE_ROW), expert_num_tokens, max_tokens};
+    return run_mlp(plan, MOE_KERNEL_L1, d.fmt, d.E, d.I, d.H, false, R(B_XQ), R(B_XSF), L.rows, weights, meta + 1, 0,
+                   L.tiles, (const int*)R(B_TILE_EXPERT), nullptr, 0, (const float*)R(B_XSCALE), l2_act_scale,
+                   R(B_HQ), R(B_HSF), nullptr, (__nv_bfloat16*)out, err, true, sched, st, &br);
 }
 
 int moe_last_status(moe_plan_t plan, void* workspace, void* stream, int32_t* status) {

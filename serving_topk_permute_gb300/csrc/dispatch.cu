@@ -60,9 +60,9 @@ __device__ __forceinline__ int mxfp8_block_exponent(const float (&f)[8]) {
     return ue8m0_exponent(amax);
 }
 
-__global__ void __launch_bounds__(DISPATCH_THREADS, 3)
-    dispatch_kernel(const DispatchArgs a) {
-    const int t = blockIdx.x;
+// One token (routed layout: written to its k permuted rows) or one row of the batched
+// layout (batched: written to the same row).
+__device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t, const bool batched) {
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     const int nchunks = a.H / 8;
     __shared__ int s_rows[32];
@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 3)
     // chunk counts only the token's slots from that chunk's start.)
     const int R = a.T * a.k, chunk = route_chunk(R);
     const int s0 = t * a.k, c0 = s0 / chunk * chunk;
+    if (!batched) {
     if (tid < a.k) {
         s_exp[tid] = __ldcg(a.ids + s0 + tid);
         s_rank[tid] = 0;
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 3)
         for (int j = 0; j < tid; ++j) n += s_exp[j] == e && (s0 + j) / chunk == my_chunk;
         s_rank[tid] = n;  // only this thread reads it back (after the next barrier)
     }
+    }  // !batched
 
     // NVFP4: the token's own scale
     float gs = 1.0f;
@@ -149,7 +151,9 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 3)
     grid_dep_wait();  // routing has written the chunk bases (and the previous forward is done with x_scale)
     grid_dep_launch();
     if (a.fmt == MOE_FMT_NVFP4 && tid == 0) a.x_scale[t] = gs;
-    if (tid < a.k) {
+    if (batched) {
+        if (tid == 0) s_rows[0] = t;
+    } else if (tid < a.k) {
         const int s = t * a.k + tid, e = s_exp[tid];
         const int r = e >= 0 && e < a.E ? a.wbase[s / chunk * a.E + e] + s_rank[tid] : -1;
         a.inv[s] = r;
@@ -157,7 +161,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 3)
         if (r >= 0) a.src[r] = s;  // the routing kernel wrote the padding rows
     }
     __syncthreads();
-    const int k = a.k;
+    const int k = batched ? 1 : a.k;
     const int64_t nks_x = fmt_k_stages(a.fmt, a.H);
 
 #pragma unroll
@@ -225,7 +229,8 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 3)
                 }
         }
         // unpermuted copy for the shared expert
-        if (a.shared_fmt == MOE_FMT_BF16) {
+        if (batched) {
+        } else if (a.shared_fmt == MOE_FMT_BF16) {
             if (in) reinterpret_cast<uint4*>(a.sxq + (int64_t)t * a.H * 2)[c] = v[i];
         } else if (a.shared_fmt == MOE_FMT_MXFP8) {
             const int ex = mxfp8_block_exponent(f);
@@ -237,11 +242,29 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 3)
             }
         }
     }
+    if (batched) __syncthreads();  // the next row reuses the shared arrays
+}
+
+__global__ void __launch_bounds__(DISPATCH_THREADS, 3) dispatch_kernel(const DispatchArgs a) {
+    if (!a.batch_counts) {
+        dispatch_one(a, blockIdx.x, false);
+        return;
+    }
+    // batched layout: a.T = E * M rows, strided over the grid; row r = e * M + m is used
+    // when m < batch_counts[e] (an input: complete before this kernel starts)
+    for (int r = blockIdx.x; r < a.T; r += gridDim.x) {
+        const int e = r / a.batch_M;
+        if (r - e * a.batch_M >= __ldcg(a.batch_counts + e)) continue;  // uniform across the CTA
+        dispatch_one(a, r, true);
+    }
+    grid_dep_wait();  // (returns at once if a row above already waited)
+    grid_dep_launch();
 }
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl) {
     LaunchAttrs at(pdl);
-    cudaLaunchConfig_t cfg = at.config(dim3(a.T), dim3(DISPATCH_THREADS), 0, st);
+    const int grid = a.batch_counts ? (a.T < 2048 ? a.T : 2048) : a.T;
+    cudaLaunchConfig_t cfg = at.config(dim3(grid), dim3(DISPATCH_THREADS), 0, st);
     return cudaLaunchKernelEx(&cfg, dispatch_kernel, a);
 }
 

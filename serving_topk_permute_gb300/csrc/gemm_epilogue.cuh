@@ -30,6 +30,10 @@ __device__ __forceinline__ bool row_valid(const GemmArgs& p, int row, int* token
         return s >= 0;
     }
     *token = row;
+    if (p.counts) {
+        const int e = row / p.rows_per_expert;
+        return row - e * p.rows_per_expert < __ldg(p.counts + e);
+    }
     return row < p.m_valid;
 }
 

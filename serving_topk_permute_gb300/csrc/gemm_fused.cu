@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const CUtensorMap* tmA = l1 ? &tmA1 : &tmA2;
                 const CUtensorMap* tmB = l1 ? &tmB1 : &tmB2;
                 const int e = p1.tile_expert ? p1.tile_expert[mt] : 0;
+                const int row0 = p1.tile_row ? p1.tile_row[mt] : mt * BM;  // a multiple of 128
                 if (!l1) {
                     // the L2 input of this row tile is complete once every L1 epilogue warp published it
                     if (!flag_wait_geq(fs.done + mt, done_target, tmo, abort_flag)) {
@@ -190,11 +191,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     }
                     const uint32_t st = smem_u32(smem + stage * C::STAGE_BYTES);
                     mbar_arrive_expect_tx(full, C::TX_BYTES);
-                    tma_load_2d(st, tmA, full, ks * BK_BYTES, mt * BM);
+                    tma_load_2d(st, tmA, full, ks * BK_BYTES, row0);
                     tma_load_3d(st + C::A_BYTES, tmB, full, ks * BK_BYTES, nt * BN, e);
                     if constexpr (S > 0) {
-                        bulk_load(st + C::A_BYTES + C::B_BYTES, p.sfa + ((int64_t)mt * p.nks + ks) * C::SFA_BYTES,
-                                  C::SFA_BYTES, full);
+                        bulk_load(st + C::A_BYTES + C::B_BYTES,
+                                  p.sfa + ((int64_t)(row0 / BM) * p.nks + ks) * C::SFA_BYTES, C::SFA_BYTES, full);
                         const int64_t blk = ((int64_t)e * p.nks + ks) * p.sf_blocks + (int64_t)nt * NB;
                         bulk_load(st + C::A_BYTES + C::B_BYTES + C::SFA_BYTES, p.sfb + blk * S * ATOM_BYTES,
                                   C::SFB_BYTES, full);
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             tc_fence_after();
             const int e = p1.tile_expert ? p1.tile_expert[mt] : 0;
-            const int row = mt * BM + q * 32 + lane;
+            const int row = (p1.tile_row ? p1.tile_row[mt] : mt * BM) + q * 32 + lane;
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16);
             // hand the accumulator back as soon as it sits in registers
             auto release = [&]() {

@@ -54,6 +54,12 @@ cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int bm, int* c
                          int* tile_expert, int* meta, int* err, cudaStream_t st, bool pdl = false,
                          uint32_t* zero = nullptr, int n_zero = 0, int* wbase = nullptr);
 
+// Batched (masked) layout: the row tiles holding used rows (counts[e] of expert e's
+// M-row slab), in expert order: tile_expert[], tile_row[] (first row), meta[1] = number
+// of tiles. Also zeroes err and zero[0..n_zero). One CTA; E <= 1024.
+cudaError_t launch_batched_plan(const int32_t* counts, int E, int M, int* tile_expert, int* tile_row, int* meta,
+                                int* err, uint32_t* zero, int n_zero, cudaStream_t st, bool pdl = false);
+
 // ------------------------------------------------------------------ dispatch quantisation
 struct DispatchArgs {
     const uint16_t* x;   // bf16 bits [T, H]
@@ -70,6 +76,10 @@ struct DispatchArgs {
     int shared_fmt;      // -1: no shared copy
     uint8_t* sxq;        // [T_pad, H/vpe] identity rows
     uint8_t* sxsf;
+    // batched layout (when batch_counts is set): T = E * batch_M rows, row e * M + m used
+    // when m < batch_counts[e], quantised into the same row; no ranks, no shared copy
+    const int* batch_counts;
+    int batch_M;
 };
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl = false);
 
@@ -84,8 +94,11 @@ struct GemmArgs {
     const int* m_tiles_dev;    // number of 128-row tiles on the device (or null)
     int m_tiles_host;          // used when m_tiles_dev is null
     const int* tile_expert;    // expert of each row tile (null: expert 0)
-    const int* src;            // flat slot of each row, -1 = padding (null: rows < m_valid are valid)
+    const int* tile_row;       // first row of each row tile (null: tile * 128)
+    const int* src;            // flat slot of each row, -1 = padding (null: see counts, else rows < m_valid)
     int m_valid;
+    const int* counts;         // batched layout: row r is used when r % rows_per_expert < counts[r / rows_per_expert]
+    int rows_per_expert;
     int top_k;
     const float* x_scale;      // NVFP4 L1: per-token dispatch scale [T]
     const float* gscale;       // NVFP4: per-expert global weight scale [E]

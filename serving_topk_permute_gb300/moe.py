@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
             "moe_plan_kernel_times": [P, P, I32],
             "moe_permute_noalloc": [P, I32, I32, I32, P, P, P],
             "moe_plan_set_wait_timeout": [P, ctypes.c_uint64],
+            "moe_batched_workspace_size": [P, I32, P],
+            "moe_forward_batched": [P, I32, P, P, P, P, P, P, SZ, P],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -264,6 +266,27 @@ class Plan:
             self._h, T, _ptr(hidden), _ptr(topk_ids), _ptr(topk_weights), ctypes.byref(w), _ptr(l2_act_scale),
             ctypes.byref(sh) if sh is not None else None, _ptr(norm_gamma), _ptr(out), _ptr(workspace),
             workspace.numel(), _stream(stream)))
+        return out
+
+    def batched_workspace_size(self, max_tokens: int) -> int:
+        n = ctypes.c_size_t()
+        _check("moe_batched_workspace_size", lib().moe_batched_workspace_size(self._h, max_tokens, ctypes.byref(n)))
+        return n.value
+
+    def forward_batched(self, hidden: torch.Tensor, expert_num_tokens: torch.Tensor, weights: dict,
+                        l2_act_scale: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """moe_forward_batched: hidden bf16 [E, M, H] with expert_num_tokens int32 [E] -> out bf16
+        [E, M, H] (rows m >= expert_num_tokens[e] are not written)."""
+        E, M, _ = hidden.shape
+        if out is None:
+            out = torch.zeros_like(hidden)
+        if workspace is None:
+            workspace = torch.zeros(self.batched_workspace_size(M), dtype=torch.uint8, device=hidden.device)
+        w = _weights_struct(weights)
+        _check("moe_forward_batched", lib().moe_forward_batched(
+            self._h, M, _ptr(hidden), _ptr(expert_num_tokens), ctypes.byref(w), _ptr(l2_act_scale), _ptr(out),
+            _ptr(workspace), workspace.numel(), _stream(stream)))
         return out
 
     def set_wait_timeout(self, ns: int):

@@ -355,6 +355,62 @@ def test_activation_variants(alpha, beta, clamp):
     G.assert_close(G.out_f64(G.run_gpu(case)), G.oracle_out(case), "mxfp8", "activation")
 
 
+# ----------------------------------------------------------------------------- batched (masked) layout
+
+def _batched_case(fmt, E=6, M=256):
+    H, I = (512, 256) if fmt in ("nvfp4", "mxfp4", "bf16") else (384, 256)
+    shape = _small_case(fmt, E=E, H=H, I=I, k=1, T=8)
+    case = G.float_case(shape)
+    xb = S.hidden_states(S.shrink(shape, T=E * M)).reshape(E, M, H)
+    import serving_topk_permute_gb300 as pkg
+    plan = pkg.Plan(G.layer_config(case))
+    kw = plan.transform_weights(G._ckpt_dev(case.layer.routed))
+    a2 = torch.tensor([np.float32(case.layer.a2)], device=G.dev()) if fmt == "nvfp4" else None
+    return case, xb, plan, kw, a2
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4", "mxfp4"])
+def test_batched_layout_matches_oracle(fmt):
+    """moe_forward_batched on [E, M, H] slabs: used rows (counts 0, 1, a whole tile, a tile
+    plus one, the whole slab, a ragged one) within tolerance of the oracle; other rows untouched."""
+    E, M = 6, 256
+    case, xb, plan, kw, a2 = _batched_case(fmt, E, M)
+    counts = np.array([0, 1, 128, 129, 256, 37], np.int32)
+    out = torch.full((E, M, xb.shape[2]), 7.0, dtype=torch.bfloat16, device=G.dev())
+    ws = torch.zeros(plan.batched_workspace_size(M), dtype=torch.uint8, device=G.dev())
+    plan.forward_batched(G.bf16_dev(xb.reshape(E * M, -1)).view(E, M, -1), G.to_dev(counts), kw, l2_act_scale=a2,
+                         out=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert plan.last_status(ws) == 0
+    want = OM.forward_batched(case.layer, xb, counts, exact=True)
+    got = out.float().cpu().numpy().astype(np.float64)
+    used = np.arange(M)[None, :] < counts[:, None]
+    G.assert_close(got[used], want[used], fmt, "batched")
+    assert np.all(got[~used] == 7.0)
+
+
+def test_batched_layout_errors():
+    """max_tokens not a multiple of 128 is refused; a count above max_tokens is clamped and
+    reported as MOE_ERR_CAPACITY; a plan on CTA pairs cannot run the batched layout."""
+    import serving_topk_permute_gb300 as pkg
+    E, M = 6, 256
+    case, xb, plan, kw, a2 = _batched_case("mxfp8", E, M)
+    with pytest.raises(pkg.MoeError):
+        plan.batched_workspace_size(200)
+    counts = np.array([3, 300, 0, 5, 256, 1], np.int32)
+    ws = torch.zeros(plan.batched_workspace_size(M), dtype=torch.uint8, device=G.dev())
+    out = plan.forward_batched(G.bf16_dev(xb.reshape(E * M, -1)).view(E, M, -1), G.to_dev(counts), kw, workspace=ws)
+    torch.cuda.synchronize()
+    assert plan.last_status(ws) == 3  # MOE_ERR_CAPACITY
+    clamped = np.minimum(counts, M)
+    want = OM.forward_batched(case.layer, xb, clamped, exact=True)
+    used = np.arange(M)[None, :] < clamped[:, None]
+    G.assert_close(out.float().cpu().numpy().astype(np.float64)[used], want[used], "mxfp8", "clamped")
+    pair = pkg.Plan(G.layer_config(case, cta="pair"))
+    with pytest.raises(pkg.MoeError):
+        pair.batched_workspace_size(M)
+
+
 # ----------------------------------------------------------------------------- weight layout
 
 def _expected_interleave(w13: np.ndarray, I: int) -> np.ndarray:
