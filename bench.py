@@ -350,6 +350,31 @@ def run_ours(args, shape: S.MoeShape):
     def step():
         plan.forward(hidden, tid, tw, kw, l2_act_scale=a2, shared=ks, norm_gamma=gamma, out=out, workspace=ws)
 
+    host_inputs = [x, ids, w]
+    if args.batched:
+        # the same routed rows on the batched (masked) layout: expert e's slots, in slot order, in its
+        # own slab of M rows (M = the largest count rounded up to 128); no combine
+        if shape.shared_I or shape.post_norm:
+            raise SystemExit("--batched: the batched layout has no shared expert and no norm")
+        flat = ids.reshape(-1)
+        counts = np.bincount(flat[flat >= 0], minlength=shape.E).astype(np.int32)
+        M = max(128, -(-int(counts.max()) // 128) * 128)
+        xb = np.zeros((shape.E, M, shape.H), np.uint16)
+        fill = np.zeros(shape.E, np.int64)
+        for slot in range(flat.size):
+            e = int(flat[slot])
+            if e >= 0:
+                xb[e, fill[e]] = x[slot // shape.k]
+                fill[e] += 1
+        hidden = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+        cnt_d = torch.from_numpy(counts).to(dev)
+        out = torch.zeros_like(hidden)
+        ws = torch.zeros(plan.batched_workspace_size(M), dtype=torch.uint8, device=dev)
+        host_inputs = [xb, counts]
+
+        def step():
+            plan.forward_batched(hidden, cnt_d, kw, l2_act_scale=a2, out=out, workspace=ws)
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -362,7 +387,7 @@ def run_ours(args, shape: S.MoeShape):
     with torch.cuda.graph(graph):
         step()
     torch.cuda.synchronize()
-    kernels_per_step = 5 + (2 if shape.shared_I else 0)
+    kernels_per_step = 3 if args.batched else 5 + (2 if shape.shared_I else 0)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
@@ -402,21 +427,20 @@ def run_ours(args, shape: S.MoeShape):
     plan.enable_timing(False)
 
     # ---- end to end: pinned host inputs -> device -> forward -> host output, every step. The step's
-    # inputs (hidden, ids, weights) sit in one pinned staging buffer and go over in one copy into one
-    # device buffer, whose 256-byte-aligned slices the forward reads.
-    nb_h, nb_i, nb_w = x.nbytes, ids.nbytes, w.nbytes
-    off_i = -(-nb_h // 256) * 256
-    off_w = off_i + -(-nb_i // 256) * 256
-    h_stage = torch.empty(off_w + nb_w, dtype=torch.uint8).pin_memory()
-    h_stage[:nb_h].copy_(torch.from_numpy(x.view(np.uint8).reshape(-1)))
-    h_stage[off_i:off_i + nb_i].copy_(torch.from_numpy(np.ascontiguousarray(ids).view(np.uint8).reshape(-1)))
-    h_stage[off_w:off_w + nb_w].copy_(torch.from_numpy(np.ascontiguousarray(w).view(np.uint8).reshape(-1)))
+    # inputs (hidden, ids, weights; or the batched slabs and counts) sit in one pinned staging buffer and
+    # go over in one copy into one device buffer, whose 256-byte-aligned slices the forward reads.
+    offs, o = [], 0
+    for arr in host_inputs:
+        offs.append(o)
+        o += -(-arr.nbytes // 256) * 256
+    h_stage = torch.empty(o, dtype=torch.uint8).pin_memory()
+    for arr, off in zip(host_inputs, offs):
+        h_stage[off:off + arr.nbytes].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1)))
     d_stage = torch.empty_like(h_stage, device=dev)
-    e_hidden = d_stage[:nb_h].view(torch.bfloat16).view(T, shape.H)
-    e_ids = d_stage[off_i:off_i + nb_i].view(torch.int32).view(ids.shape)
-    e_w = d_stage[off_w:off_w + nb_w].view(torch.float32).view(w.shape)
-    e_out = torch.empty_like(hidden)
-    h_out = torch.empty((T, shape.H), dtype=torch.int16).pin_memory()
+    torch_dt = {np.dtype(np.uint16): torch.bfloat16, np.dtype(np.int32): torch.int32, np.dtype(np.float32): torch.float32}
+    e_in = [d_stage[off:off + arr.nbytes].view(torch_dt[arr.dtype]).view(arr.shape) for arr, off in zip(host_inputs, offs)]
+    e_out = torch.zeros_like(out)
+    h_out = torch.empty(out.shape, dtype=torch.int16).pin_memory()
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
@@ -424,7 +448,11 @@ def run_ours(args, shape: S.MoeShape):
         flush(i)
         e2e_ev[i][0].record()
         d_stage.copy_(h_stage, non_blocking=True)
-        plan.forward(e_hidden, e_ids, e_w, kw, l2_act_scale=a2, shared=ks, norm_gamma=gamma, out=e_out, workspace=ws)
+        if args.batched:
+            plan.forward_batched(e_in[0], e_in[1], kw, l2_act_scale=a2, out=e_out, workspace=ws)
+        else:
+            plan.forward(e_in[0], e_in[1], e_in[2], kw, l2_act_scale=a2, shared=ks, norm_gamma=gamma, out=e_out,
+                         workspace=ws)
         h_out.copy_(e_out.view(torch.int16), non_blocking=True)
         e2e_ev[i][1].record()
     torch.cuda.synchronize()
@@ -432,7 +460,7 @@ def run_ours(args, shape: S.MoeShape):
     assert torch.equal(e_out.view(torch.int16), out.view(torch.int16)), "end-to-end output differs from the graph's"
     e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev))
     e2e_value = world * T * args.steps / (e2e_ms / 1e3)
-    h2d = nb_h + nb_i + nb_w
+    h2d = sum(arr.nbytes for arr in host_inputs)
     d2h = h_out.numel() * 2
     if plan.last_status(ws) != 0:
         raise RuntimeError("device status after timing")
@@ -475,6 +503,8 @@ def run_ours(args, shape: S.MoeShape):
         "data": "synthetic (seeded activations and routing; checkpoint bytes drawn on the device)",
         "config": {**workload_config(shape, world), "launch": "serial" if args.serial else "programmatic dependent launch",
                    "tile": args.tile or "library", "cta": args.cta, "gemm": "split" if args.split_gemm else "library",
+                   **({"layout": f"batched [E, M, H], M = {out.shape[1]} (tokens/s counts the workload's T tokens, "
+                                 f"whose k routed rows the slabs hold; no combine)"} if args.batched else {}),
                    **({"l2": "flushed before every timed step (256 MB write only)"} if args.flush_write_only else {})},
         "roofline": rl,
         "layer": {"tflops": round(work["flops"] / sec / 1e12, 2), "hbm_gbs": round(work["bytes"] / sec / 1e9, 1),
@@ -509,6 +539,8 @@ def main(argv=None):
     ap.add_argument("--cta", choices=["auto", "pair", "single"], default="auto",
                     help="GEMMs on CTA pairs: the library's choice, always or never")
     ap.add_argument("--split-gemm", action="store_true", help="L1 and L2 as two kernels instead of one")
+    ap.add_argument("--batched", action="store_true",
+                    help="the workload's routed rows on the batched [E, M, H] layout (moe_forward_batched)")
     ap.add_argument("--flush-write-only", action="store_true",
                     help="flush the L2 with the 256 MB write alone (its dirty lines are written back inside the step)")
     ap.add_argument("--serial", action="store_true",

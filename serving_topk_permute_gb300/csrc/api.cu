@@ -608,7 +608,8 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
 
 // ------------------------------------------------------------------ batched (masked) layout
 namespace {
-enum BRegion { B_ERR, B_META, B_TILE_EXPERT, B_TILE_ROW, B_XQ, B_XSF, B_XSCALE, B_HQ, B_HSF, B_SCHED, B_COUNT };
+enum BRegion { B_ERR, B_META, B_TILE_EXPERT, B_TILE_ROW, B_ROW_PREFIX, B_XQ, B_XSF, B_XSCALE, B_HQ, B_HSF, B_SCHED,
+               B_COUNT };
 struct BLayout {
     int64_t off[B_COUNT];
     int64_t size[B_COUNT];
@@ -626,6 +627,7 @@ BLayout batched_layout_of(const moe_config_t& c, int M) {
     sz[B_META] = 16;
     sz[B_TILE_EXPERT] = 4 * L.tiles;
     sz[B_TILE_ROW] = 4 * L.tiles;
+    sz[B_ROW_PREFIX] = 4 * (d.E + 1);
     sz[B_XQ] = L.rows * fmt_row_bytes(d.fmt, d.H);
     sz[B_XSF] = L.tiles * fmt_k_stages(d.fmt, d.H) * S * ATOM_BYTES;
     sz[B_XSCALE] = 4 * L.rows;
@@ -685,7 +687,7 @@ int moe_forward_batched(moe_plan_t plan, int32_t max_tokens, const void* hidden,
     {
         KernelTimer kt(plan, MOE_KERNEL_ROUTE, st);
         CUDA_TRY(launch_batched_plan(expert_num_tokens, d.E, max_tokens, (int*)R(B_TILE_EXPERT), (int*)R(B_TILE_ROW),
-                                     meta, err, sched, (int)(1 + L.tiles), st, plan->pdl));
+                                     (int*)R(B_ROW_PREFIX), meta, err, sched, (int)(1 + L.tiles), st, plan->pdl));
     }
     DispatchArgs da{};
     da.x = (const uint16_t*)hidden;
@@ -699,6 +701,7 @@ int moe_forward_batched(moe_plan_t plan, int32_t max_tokens, const void* hidden,
     da.x_scale = (float*)R(B_XSCALE);
     da.shared_fmt = -1;
     da.batch_counts = expert_num_tokens;
+    da.batch_prefix = (const int*)R(B_ROW_PREFIX);
     da.batch_M = max_tokens;
     {
         KernelTimer kt(plan, MOE_KERNEL_DISPATCH, st);

@@ -250,15 +250,23 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 3) dispatch_kernel(const Dis
         dispatch_one(a, blockIdx.x, false);
         return;
     }
-    // batched layout: a.T = E * M rows, strided over the grid; row r = e * M + m is used
-    // when m < batch_counts[e] (an input: complete before this kernel starts)
-    for (int r = blockIdx.x; r < a.T; r += gridDim.x) {
-        const int e = r / a.batch_M;
-        if (r - e * a.batch_M >= __ldcg(a.batch_counts + e)) continue;  // uniform across the CTA
-        dispatch_one(a, r, true);
-    }
-    grid_dep_wait();  // (returns at once if a row above already waited)
+    // batched layout: the used rows, numbered 0 .. batch_prefix[E) in expert order, strided
+    // over the grid; used row i is row e * M + (i - batch_prefix[e]) of the expert e with
+    // batch_prefix[e] <= i < batch_prefix[e + 1]
+    grid_dep_wait();  // the planning kernel has written batch_prefix
     grid_dep_launch();
+    const int used = a.batch_prefix[a.E];
+    for (int i = blockIdx.x; i < used; i += gridDim.x) {
+        int lo = 0, hi = a.E;  // batch_prefix[lo] <= i < batch_prefix[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) / 2;
+            if (a.batch_prefix[mid] <= i)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        dispatch_one(a, lo * a.batch_M + (i - a.batch_prefix[lo]), true);
+    }
 }
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl) {

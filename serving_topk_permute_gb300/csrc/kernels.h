@@ -56,9 +56,11 @@ cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int bm, int* c
 
 // Batched (masked) layout: the row tiles holding used rows (counts[e] of expert e's
 // M-row slab), in expert order: tile_expert[], tile_row[] (first row), meta[1] = number
-// of tiles. Also zeroes err and zero[0..n_zero). One CTA; E <= 1024.
-cudaError_t launch_batched_plan(const int32_t* counts, int E, int M, int* tile_expert, int* tile_row, int* meta,
-                                int* err, uint32_t* zero, int n_zero, cudaStream_t st, bool pdl = false);
+// of tiles; row_prefix[E+1] = used rows of the experts before e. Also zeroes err and
+// zero[0..n_zero). One CTA; E <= 1024.
+cudaError_t launch_batched_plan(const int32_t* counts, int E, int M, int* tile_expert, int* tile_row,
+                                int* row_prefix, int* meta, int* err, uint32_t* zero, int n_zero, cudaStream_t st,
+                                bool pdl = false);
 
 // ------------------------------------------------------------------ dispatch quantisation
 struct DispatchArgs {
@@ -77,8 +79,10 @@ struct DispatchArgs {
     uint8_t* sxq;        // [T_pad, H/vpe] identity rows
     uint8_t* sxsf;
     // batched layout (when batch_counts is set): T = E * batch_M rows, row e * M + m used
-    // when m < batch_counts[e], quantised into the same row; no ranks, no shared copy
+    // when m < batch_counts[e], quantised into the same row; no ranks, no shared copy.
+    // batch_prefix[E+1] (from the planning kernel): used rows of the experts before e.
     const int* batch_counts;
+    const int* batch_prefix;
     int batch_M;
 };
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl = false);

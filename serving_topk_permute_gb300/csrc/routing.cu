@@ -188,8 +188,8 @@ namespace moe {
 // counts[e] rows are used, so it contributes ceil(counts[e] / 128) row tiles. One CTA.
 __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     batched_plan_kernel(const int32_t* __restrict__ counts, int E, int M, int* __restrict__ tile_expert,
-                        int* __restrict__ tile_row, int* __restrict__ meta, int* err, uint32_t* __restrict__ zero,
-                        int n_zero) {
+                        int* __restrict__ tile_row, int* __restrict__ row_prefix, int* __restrict__ meta, int* err,
+                        uint32_t* __restrict__ zero, int n_zero) {
     __shared__ int s_wsum[ROUTE_WARPS];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     grid_dep_wait();  // the previous kernel (which may still read the tile lists) has finished
@@ -197,9 +197,9 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
     if (tid == 0 && err) *err = 0;
     for (int i = tid; i < n_zero; i += ROUTE_THREADS) zero[i] = 0u;
     __syncthreads();
-    int n = 0;
+    int n = 0, c = 0;
     if (tid < E) {
-        int c = counts[tid];
+        c = counts[tid];
         if (c < 0 || c > M) {
             set_error(err, MOE_ERR_CAPACITY);
             c = c < 0 ? 0 : M;
@@ -234,13 +234,39 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1)
         meta[0] = incl * BM;
         meta[1] = incl;
     }
+    // the same scan over the used rows: row_prefix[e] = used rows of experts before e, so
+    // the dispatch kernel can spread the used rows evenly over its CTAs
+    __syncthreads();
+    x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = s_wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        s_wsum[lane] = w;
+    }
+    __syncthreads();
+    const int rincl = x + (warp > 0 ? s_wsum[warp - 1] : 0);
+    if (tid < E) row_prefix[tid] = rincl - c;
+    if (tid == E - 1) row_prefix[E] = rincl;
 }
 
-cudaError_t launch_batched_plan(const int32_t* counts, int E, int M, int* tile_expert, int* tile_row, int* meta,
-                                int* err, uint32_t* zero, int n_zero, cudaStream_t st, bool pdl) {
+cudaError_t launch_batched_plan(const int32_t* counts, int E, int M, int* tile_expert, int* tile_row,
+                                int* row_prefix, int* meta, int* err, uint32_t* zero, int n_zero, cudaStream_t st,
+                                bool pdl) {
     LaunchAttrs at(pdl);
     cudaLaunchConfig_t cfg = at.config(dim3(1), dim3(ROUTE_THREADS), 0, st);
-    return cudaLaunchKernelEx(&cfg, batched_plan_kernel, counts, E, M, tile_expert, tile_row, meta, err, zero, n_zero);
+    return cudaLaunchKernelEx(&cfg, batched_plan_kernel, counts, E, M, tile_expert, tile_row, row_prefix, meta, err,
+                              zero, n_zero);
 }
 
 }  // namespace moe
