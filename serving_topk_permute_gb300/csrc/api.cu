@@ -422,19 +422,22 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool p
                    const moe_weights_t* w, const int* m_tiles_dev, int m_tiles_host, int64_t m_tiles_max,
                    const int* tile_expert, const int* src, int m_valid, const float* x_scale, const float* a2,
                    uint8_t* hq, uint8_t* hsf, float* h_debug, __nv_bfloat16* y, int* err, bool activation,
-                   uint32_t* sched, cudaStream_t st, const BatchRows* br = nullptr) {
+                   uint32_t* sched, cudaStream_t st, const BatchRows* br = nullptr,
+                   const int* seg_off = nullptr, const int* seg_cnt = nullptr) {
     const moe_config_t& c = p->cfg;
     const int S = fmt_sf_atoms(fmt);
     const int bn = pair ? 2 * BM : choose_bn(c, 0);
     const uint32_t b_box = pair ? NBLK : bn;  // a CTA of a pair loads half of the 256 weight rows
     const bool fused = !pair && bn == 256 && sched && !(c.flags & MOE_FLAG_SPLIT_GEMM);
-    CUtensorMap ta1, tb1, ta2, tb2, tsa1, tsb1, tsa2, tsb2;
+    CUtensorMap ta1, tb1, ta2, tb2, tsa1, tsb1, tsa2, tsb2, ta1s, ta2s;
     GemmArgs g{};
     g.m_tiles_dev = m_tiles_dev;
     g.m_tiles_host = m_tiles_host;
     g.tile_expert = tile_expert;
     g.src = src;
     g.m_valid = m_valid;
+    g.seg_off = seg_off;
+    g.seg_cnt = seg_cnt;
     if (br) {
         g.tile_row = br->tile_row;
         g.counts = br->counts;
@@ -486,11 +489,14 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool p
         if (!map_atoms(&tsb2, w->w2_sf, (uint64_t)E * g2.nks * g2.sf_blocks * S, sfb_box)) return MOE_ERR_CUDA;
     }
     if (fused) {
+        // the one-kernel GEMM loads mostly empty row tiles in smaller boxes
+        if (!map_2d(&ta1s, xq, fmt_row_bytes(fmt, H), rows, A_BOX_ROWS)) return MOE_ERR_CUDA;
+        if (!map_2d(&ta2s, hq, fmt_row_bytes(fmt, I), rows, A_BOX_ROWS)) return MOE_ERR_CUDA;
         FusedSched fs{sched, sched + 1};
         const int64_t tiles = m_tiles_max * (g1.n_tiles + g2.n_tiles);
         const int grid = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, tiles));
         KernelTimer kt(p, kid1, st);
-        CUDA_TRY(launch_fused_mlp(fmt, ta1, tb1, ta2, tb2, g1, g2, fs, grid, st, p->pdl));
+        CUDA_TRY(launch_fused_mlp(fmt, ta1, tb1, ta2, tb2, ta1s, ta2s, g1, g2, fs, grid, st, p->pdl));
         return MOE_OK;
     }
     auto launch = [&](bool l1, const GemmArgs& ga, int64_t tiles) {
@@ -578,7 +584,8 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
                      meta + 1, 0, L.m_pad_max / bm,
                      (const int*)R(R_TILE_EXPERT), (const int*)R(R_SRC), 0, (const float*)R(R_XSCALE), l2_act_scale,
                      R(R_HQ), R(R_HSF), (c.flags & MOE_FLAG_DEBUG_H) ? (float*)R(R_HDBG) : nullptr,
-                     (__nv_bfloat16*)R(R_Y), err, true, (uint32_t*)R(R_SCHED), st);
+                     (__nv_bfloat16*)R(R_Y), err, true, (uint32_t*)R(R_SCHED), st, nullptr, (const int*)R(R_OFF),
+                     (const int*)R(R_CNT));
     if (rc != MOE_OK) return rc;
     if (d.Is > 0) {
         const bool shared_pair = use_pair(c, T);

@@ -18,6 +18,7 @@ constexpr int BM = 128;            // rows per MMA tile (= BLOCK_M of the routin
 constexpr int BN_MAX = 256;        // widest MMA tile (weight rows); tiles are 128 or 256 wide
 constexpr int NBLK = 128;          // weight rows per scale-atom block and per gate/up interleave unit
 constexpr int BK_BYTES = 128;      // bytes of codes per K stage (one 128-byte swizzle row)
+constexpr int A_BOX_ROWS = 32;     // the one-kernel GEMM loads a row tile's used rows in boxes this high
 constexpr int ATOM_BYTES = 512;    // one scale-factor atom: 128 rows x 4 scales
 constexpr int EPI_WARPS = 16;      // 4 per tensor-memory lane quarter, each on a quarter of the columns
 constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA producer, warp 1 MMA issuer, then epilogue

@@ -56,10 +56,18 @@ struct FusedCfg {
     static_assert(NUM_BARS * 8 + (TRING + 4) * 4 <= BAR_BYTES, "barrier area");
 };
 
+// Row tiles are taken alternately from the front and the back of the expert order
+// (0, M-1, 1, M-2, ...). Under skewed routing the front holds the large experts, whose
+// tiles reuse their weights from L2 and keep the tensor cores busy, and the back the
+// small ones, whose tiles stream their weights from HBM once; alternating runs both
+// kinds at the same time instead of one phase after the other. A bijection on [0, M).
+__device__ __forceinline__ int interleave_tile(int i, int m) { return (i & 1) ? m - 1 - (i >> 1) : (i >> 1); }
+
 template <int FMT>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     fused_mlp_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                      const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                     const __grid_constant__ CUtensorMap tmA1s, const __grid_constant__ CUtensorMap tmA2s,
                      const GemmArgs p1, const GemmArgs p2, const FusedSched fs) {
     using C = FusedCfg<FMT>;
     constexpr int S = C::S, NB = C::NB, STAGES = C::STAGES, BN = C::BN, TRING = C::TRING;
@@ -100,6 +108,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         prefetch_tmap(&tmB1);
         prefetch_tmap(&tmA2);
         prefetch_tmap(&tmB2);
+        prefetch_tmap(&tmA1s);
+        prefetch_tmap(&tmA2s);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -124,7 +134,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         first = (int)atomicAdd(fs.counter, 1u);
         if (first < total1) {
-            const int mt = first / p1.n_tiles, nt = first % p1.n_tiles;
+            const int mt = interleave_tile(first / p1.n_tiles, m_tiles), nt = first % p1.n_tiles;
             const int e = p1.tile_expert ? __ldcg(p1.tile_expert + mt) : 0;
             for (int ks = 0; ks < p1.nks && ks < PREFETCH_STAGES; ++ks)
                 tma_prefetch_3d(&tmB1, ks * BK_BYTES, nt * BN, e);
@@ -142,7 +152,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         l1 = t < total1;
         const int u = l1 ? t : t - total1;
         const int n = l1 ? p1.n_tiles : p2.n_tiles;
-        mt = u / n;
+        mt = interleave_tile(u / n, m_tiles);
         nt = u % n;
     };
 
@@ -170,6 +180,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 decode(t, l1, mt, nt);
                 const GemmArgs& p = l1 ? p1 : p2;
                 const CUtensorMap* tmA = l1 ? &tmA1 : &tmA2;
+                const CUtensorMap* tmAs = l1 ? &tmA1s : &tmA2s;
                 const CUtensorMap* tmB = l1 ? &tmB1 : &tmB2;
                 const int e = p1.tile_expert ? p1.tile_expert[mt] : 0;
                 const int row0 = p1.tile_row ? p1.tile_row[mt] : mt * BM;  // a multiple of 128
@@ -181,6 +192,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     }
                     fence_proxy_async_global();
                 }
+                // A row tile with at most 96 used rows loads only the 32-row boxes holding
+                // them (the rest of the A tile keeps stale bytes, whose accumulator rows no
+                // epilogue stores); a fuller one loads the whole tile in one box.
+                int used = BM;
+                if (p1.seg_off) used = p1.seg_off[e] + p1.seg_cnt[e] - row0;
+                else if (p1.counts) used = p1.counts[e] - (row0 - e * p1.rows_per_expert);
+                else if (!p1.src) used = p1.m_valid - row0;
+                const bool whole = used > BM - A_BOX_ROWS;
+                const int a_boxes = whole ? 0 : (used <= A_BOX_ROWS ? 1 : (used + A_BOX_ROWS - 1) / A_BOX_ROWS);
+                const uint32_t tx =
+                    whole ? C::TX_BYTES : C::TX_BYTES - (uint32_t)(BM - a_boxes * A_BOX_ROWS) * BK_BYTES;
                 bool ok = true;
                 for (int ks = 0; ks < p.nks; ++ks) {
                     const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (STAGES + stage);
@@ -190,8 +212,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         break;
                     }
                     const uint32_t st = smem_u32(smem + stage * C::STAGE_BYTES);
-                    mbar_arrive_expect_tx(full, C::TX_BYTES);
-                    tma_load_2d(st, tmA, full, ks * BK_BYTES, row0);
+                    mbar_arrive_expect_tx(full, tx);
+                    if (whole)
+                        tma_load_2d(st, tmA, full, ks * BK_BYTES, row0);
+                    else
+                        for (int b = 0; b < a_boxes; ++b)
+                            tma_load_2d(st + b * (A_BOX_ROWS * BK_BYTES), tmAs, full, ks * BK_BYTES,
+                                        row0 + b * A_BOX_ROWS);
                     tma_load_3d(st + C::A_BYTES, tmB, full, ks * BK_BYTES, nt * BN, e);
                     if constexpr (S > 0) {
                         bulk_load(st + C::A_BYTES + C::B_BYTES,
@@ -358,21 +385,22 @@ cudaError_t fused_prepare(int fmt) {
 
 template <int FMT>
 static cudaError_t fused_t(const CUtensorMap& a1, const CUtensorMap& b1, const CUtensorMap& a2,
-                           const CUtensorMap& b2, const GemmArgs& p1, const GemmArgs& p2, const FusedSched& fs,
-                           int grid, cudaStream_t st, bool pdl) {
+                           const CUtensorMap& b2, const CUtensorMap& a1s, const CUtensorMap& a2s, const GemmArgs& p1,
+                           const GemmArgs& p2, const FusedSched& fs, int grid, cudaStream_t st, bool pdl) {
     LaunchAttrs at(pdl);
     cudaLaunchConfig_t cfg = at.config(dim3(grid), dim3(GEMM_THREADS), FusedCfg<FMT>::SMEM, st);
-    return cudaLaunchKernelEx(&cfg, fused_mlp_kernel<FMT>, a1, b1, a2, b2, p1, p2, fs);
+    return cudaLaunchKernelEx(&cfg, fused_mlp_kernel<FMT>, a1, b1, a2, b2, a1s, a2s, p1, p2, fs);
 }
 
 cudaError_t launch_fused_mlp(int fmt, const CUtensorMap& a1, const CUtensorMap& b1, const CUtensorMap& a2,
-                             const CUtensorMap& b2, const GemmArgs& p1, const GemmArgs& p2, const FusedSched& fs,
-                             int grid, cudaStream_t st, bool pdl) {
+                             const CUtensorMap& b2, const CUtensorMap& a1s, const CUtensorMap& a2s,
+                             const GemmArgs& p1, const GemmArgs& p2, const FusedSched& fs, int grid, cudaStream_t st,
+                             bool pdl) {
     switch (fmt) {
-        case MOE_FMT_BF16: return fused_t<MOE_FMT_BF16>(a1, b1, a2, b2, p1, p2, fs, grid, st, pdl);
-        case MOE_FMT_MXFP8: return fused_t<MOE_FMT_MXFP8>(a1, b1, a2, b2, p1, p2, fs, grid, st, pdl);
-        case MOE_FMT_MXFP4: return fused_t<MOE_FMT_MXFP4>(a1, b1, a2, b2, p1, p2, fs, grid, st, pdl);
-        default: return fused_t<MOE_FMT_NVFP4>(a1, b1, a2, b2, p1, p2, fs, grid, st, pdl);
+        case MOE_FMT_BF16: return fused_t<MOE_FMT_BF16>(a1, b1, a2, b2, a1s, a2s, p1, p2, fs, grid, st, pdl);
+        case MOE_FMT_MXFP8: return fused_t<MOE_FMT_MXFP8>(a1, b1, a2, b2, a1s, a2s, p1, p2, fs, grid, st, pdl);
+        case MOE_FMT_MXFP4: return fused_t<MOE_FMT_MXFP4>(a1, b1, a2, b2, a1s, a2s, p1, p2, fs, grid, st, pdl);
+        default: return fused_t<MOE_FMT_NVFP4>(a1, b1, a2, b2, a1s, a2s, p1, p2, fs, grid, st, pdl);
     }
 }
 

@@ -101,6 +101,8 @@ struct GemmArgs {
     const int* tile_row;       // first row of each row tile (null: tile * 128)
     const int* src;            // flat slot of each row, -1 = padding (null: see counts, else rows < m_valid)
     int m_valid;
+    const int* seg_off;        // routed layout: first row [E] and row count [E] of each expert's segment
+    const int* seg_cnt;        //   (null: the row tile's used rows follow from counts or m_valid)
     const int* counts;         // batched layout: row r is used when r % rows_per_expert < counts[r / rows_per_expert]
     int rows_per_expert;
     int top_k;
@@ -125,15 +127,17 @@ cudaError_t gemm_prepare(int fmt);   // sets the dynamic shared memory attribute
 
 // Both GEMMs in one persistent kernel (256-wide tiles, single CTAs). counter: the
 // next tile to take; done[m_tiles]: published L1 epilogue warps per row tile. Both
-// must be zero at launch (the routing kernel zeroes them).
+// must be zero at launch (the routing kernel zeroes them). a1/a2 load A tiles as one
+// 128-row box, a1s/a2s (same tensors) as A_BOX_ROWS-row boxes for mostly empty tiles.
 struct FusedSched {
     uint32_t* counter;
     uint32_t* done;
 };
 cudaError_t fused_prepare(int fmt);
 cudaError_t launch_fused_mlp(int fmt, const CUtensorMap& a1, const CUtensorMap& b1, const CUtensorMap& a2,
-                             const CUtensorMap& b2, const GemmArgs& p1, const GemmArgs& p2, const FusedSched& fs,
-                             int grid, cudaStream_t st, bool pdl = false);
+                             const CUtensorMap& b2, const CUtensorMap& a1s, const CUtensorMap& a2s,
+                             const GemmArgs& p1, const GemmArgs& p2, const FusedSched& fs, int grid, cudaStream_t st,
+                             bool pdl = false);
 // CTA-pair variant: 256 x 256 tiles over 256-row segments; the B map's box is 128 rows
 cudaError_t gemm2_prepare(int fmt);
 // tmSFA / tmSFB: the scale atoms as 2-D uint32 tensors [atoms][128] with boxes of
