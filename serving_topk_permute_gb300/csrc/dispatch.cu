@@ -5,8 +5,8 @@
 // deepgemm_moe_permute writes a1q_perm).
 //
 // One CTA of 256 threads per token. Each thread owns 8-element chunks
-// c = tid + 256 i of the row, loaded as one 128-bit bf16x8 vector each, kept in
-// registers. Per format:
+// c = tid + 256 i of the row (at most 4 of them for H <= 8192, 8 above), loaded as
+// one 128-bit bf16x8 vector each, kept in registers. Per format:
 //   BF16   the 16-byte chunk is copied as is
 //   MXFP8  a 32-element block is 4 neighbouring threads: block amax by two xor
 //          shuffles, e = smallest integer with amax <= 448 * 2^e, codes
@@ -28,6 +28,10 @@ namespace moe {
 
 constexpr int DISPATCH_THREADS = 256;
 constexpr int DISPATCH_MAX_CHUNKS = 8;   // H <= 8 * 256 * 8 = 16384
+// Rows of H <= 8192 use a variant holding 4 chunks per thread, which fits in 48
+// registers, so that 5 CTAs (tokens) are resident per SM instead of 3.
+constexpr int DISPATCH_SMALL_CHUNKS = 4;
+constexpr int DISPATCH_SMALL_MIN_CTAS = 5;
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -62,6 +66,7 @@ __device__ __forceinline__ int mxfp8_block_exponent(const float (&f)[8]) {
 
 // One token (routed layout: written to its k permuted rows) or one row of the batched
 // layout (batched: written to the same row).
+template <int MAXC>
 __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t, const bool batched) {
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     const int nchunks = a.H / 8;
@@ -74,10 +79,10 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
     // complete before this kernel starts (routing, the kernel before it, lets it start only
     // after its own wait for its predecessor), so they are read while routing still runs.
     // load the token's row into registers
-    uint4 v[DISPATCH_MAX_CHUNKS];
+    uint4 v[MAXC];
     const uint4* xrow = reinterpret_cast<const uint4*>(a.x + (int64_t)t * a.H);
 #pragma unroll
-    for (int i = 0; i < DISPATCH_MAX_CHUNKS; ++i) {
+    for (int i = 0; i < MAXC; ++i) {
         const int c = tid + i * DISPATCH_THREADS;
         v[i] = c < nchunks ? __ldcg(xrow + c) : make_uint4(0, 0, 0, 0);  // from L2: no stale L1 line
     }
@@ -133,7 +138,7 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
     if (a.fmt == MOE_FMT_NVFP4) {
         float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < DISPATCH_MAX_CHUNKS; ++i) {
+        for (int i = 0; i < MAXC; ++i) {
             float f[8];
             bf16x8_to_f32(v[i], f);
 #pragma unroll
@@ -165,7 +170,7 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
     const int64_t nks_x = fmt_k_stages(a.fmt, a.H);
 
 #pragma unroll
-    for (int i = 0; i < DISPATCH_MAX_CHUNKS; ++i) {
+    for (int i = 0; i < MAXC; ++i) {
         const int c = tid + i * DISPATCH_THREADS;
         if (i * DISPATCH_THREADS >= nchunks) break;  // uniform across the CTA
         const bool in = c < nchunks;
@@ -245,9 +250,10 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
     if (batched) __syncthreads();  // the next row reuses the shared arrays
 }
 
-__global__ void __launch_bounds__(DISPATCH_THREADS, 3) dispatch_kernel(const DispatchArgs a) {
+template <int MAXC, int MIN_CTAS>
+__global__ void __launch_bounds__(DISPATCH_THREADS, MIN_CTAS) dispatch_kernel(const DispatchArgs a) {
     if (!a.batch_counts) {
-        dispatch_one(a, blockIdx.x, false);
+        dispatch_one<MAXC>(a, blockIdx.x, false);
         return;
     }
     // batched layout: the used rows, numbered 0 .. batch_prefix[E) in expert order, strided
@@ -265,7 +271,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 3) dispatch_kernel(const Dis
             else
                 hi = mid;
         }
-        dispatch_one(a, lo * a.batch_M + (i - a.batch_prefix[lo]), true);
+        dispatch_one<MAXC>(a, lo * a.batch_M + (i - a.batch_prefix[lo]), true);
     }
 }
 
@@ -273,7 +279,9 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl) {
     LaunchAttrs at(pdl);
     const int grid = a.batch_counts ? (a.T < 2048 ? a.T : 2048) : a.T;
     cudaLaunchConfig_t cfg = at.config(dim3(grid), dim3(DISPATCH_THREADS), 0, st);
-    return cudaLaunchKernelEx(&cfg, dispatch_kernel, a);
+    if (a.H <= DISPATCH_SMALL_CHUNKS * DISPATCH_THREADS * 8)
+        return cudaLaunchKernelEx(&cfg, dispatch_kernel<DISPATCH_SMALL_CHUNKS, DISPATCH_SMALL_MIN_CTAS>, a);
+    return cudaLaunchKernelEx(&cfg, dispatch_kernel<DISPATCH_MAX_CHUNKS, 3>, a);
 }
 
 }  // namespace moe

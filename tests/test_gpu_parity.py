@@ -59,7 +59,10 @@ def _ids_only_case(shape):
 
 @pytest.mark.parametrize("name", S.WORKLOAD_ORDER)
 def test_routing_and_dispatch_bit_exact_full_size(name):
-    shape = W[name]
+    _check_routing_and_dispatch(W[name])
+
+
+def _check_routing_and_dispatch(shape):
     case = _ids_only_case(shape)
     run = G.run_gpu(case)
     T, k, E = shape.T, shape.k, shape.E
@@ -217,6 +220,16 @@ def test_single_token(fmt):
     shape = _small_case(fmt, T=1)
     case = G.float_case(shape)
     G.assert_close(G.out_f64(G.run_gpu(case)), G.oracle_out(case), fmt, "T=1")
+
+
+@pytest.mark.parametrize("H", [10240, 16384])
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4", "mxfp4"])
+def test_wide_hidden(fmt, H):
+    """H above 8192 (up to the 16384 limit) takes the dispatch variant holding 8 chunks per thread."""
+    shape = _small_case(fmt, T=24, H=H, I=256, E=4, k=2)
+    _check_routing_and_dispatch(shape)
+    case = G.float_case(shape)
+    G.assert_close(G.out_f64(G.run_gpu(case)), G.oracle_out(case), fmt, f"H={H}")
 
 
 def test_masked_slots_and_duplicates():
