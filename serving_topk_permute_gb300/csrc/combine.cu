@@ -5,7 +5,7 @@
 // mega_moe, finalize_weights / forward_prepared).
 //
 // One CTA per token; each thread owns 8-column chunks and handles one chunk at a
-// time: the k rows' 16-byte pieces of the chunk are loaded in batches of four
+// time: the k rows' 16-byte pieces of the chunk are loaded in batches of eight
 // (independent loads in flight), then z += w[t,j] * y[inv_perm[t,j]] in fp32 in
 // ascending j (masked slots skipped), then z += shared. Without a norm the chunk is
 // rounded to bf16 and stored at once; with the norm z goes to shared memory, the
@@ -17,7 +17,7 @@
 namespace moe {
 
 constexpr int COMBINE_THREADS = 256;
-constexpr int COMBINE_BATCH = 4;
+constexpr int COMBINE_BATCH = 8;
 
 __device__ __forceinline__ void acc_bf16x8(float (&acc)[8], const uint4& v, float w) {
     const uint32_t q[4] = {v.x, v.y, v.z, v.w};
