@@ -24,6 +24,12 @@
  *   - GPU work is enqueued on the given stream and is asynchronous; inputs
  *     must stay valid until the stream reaches the work.
  *   - Every device pointer must be 256-byte aligned (MOE_ERR_INVALID_ARG).
+ *   - moe_forward's hidden, topk_ids, topk_weights, norm_gamma and out may
+ *     also be pinned host memory mapped into the device address space
+ *     (cudaHostAlloc / cudaMallocHost under unified addressing): the routing,
+ *     dispatch and combine kernels, the only ones that touch them, then read
+ *     the inputs and write the output over the host link, with no separate
+ *     copy. Weights and the workspace must be device memory.
  *   - Bad expert ids and bounded-wait timeouts found on the device are
  *     recorded in an error word in the workspace; read it with
  *     moe_last_status (which synchronises the stream).

@@ -102,11 +102,14 @@ def _check(fn: str, status: int):
         raise MoeError(fn, status)
 
 
-def _ptr(t) -> int | None:
+def _ptr(t, host_ok: bool = False) -> int | None:
+    """Device address of t. With host_ok, a pinned CPU tensor is also accepted: under
+    unified addressing its pointer is valid on the device (the kernels access it over
+    the host link)."""
     if t is None:
         return None
-    if not t.is_cuda:
-        raise ValueError("expected a CUDA tensor")
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError("expected a CUDA tensor" + (" or a pinned CPU tensor" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError("expected a contiguous tensor")
     return t.data_ptr()
@@ -254,18 +257,23 @@ class Plan:
                 l2_act_scale: torch.Tensor | None = None, shared: dict | None = None,
                 norm_gamma: torch.Tensor | None = None, out: torch.Tensor | None = None,
                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-        """moe_forward: hidden bf16 [T, H] -> out bf16 [T, H]."""
+        """moe_forward: hidden bf16 [T, H] -> out bf16 [T, H].
+
+        hidden, topk_ids, topk_weights, norm_gamma and out may be pinned CPU tensors
+        (the kernels then read and write them in host memory directly); weights and
+        the workspace are device tensors."""
         T = hidden.shape[0]
+        dev = hidden.device if hidden.is_cuda else torch.device("cuda", torch.cuda.current_device())
         if out is None:
             out = torch.empty_like(hidden)
         if workspace is None:
-            workspace = self.alloc_workspace(T, hidden.device)
+            workspace = self.alloc_workspace(T, dev)
         w = _weights_struct(weights)
         sh = _weights_struct(shared)
         _check("moe_forward", lib().moe_forward(
-            self._h, T, _ptr(hidden), _ptr(topk_ids), _ptr(topk_weights), ctypes.byref(w), _ptr(l2_act_scale),
-            ctypes.byref(sh) if sh is not None else None, _ptr(norm_gamma), _ptr(out), _ptr(workspace),
-            workspace.numel(), _stream(stream)))
+            self._h, T, _ptr(hidden, True), _ptr(topk_ids, True), _ptr(topk_weights, True), ctypes.byref(w),
+            _ptr(l2_act_scale), ctypes.byref(sh) if sh is not None else None, _ptr(norm_gamma, True),
+            _ptr(out, True), _ptr(workspace), workspace.numel(), _stream(stream)))
         return out
 
     def batched_workspace_size(self, max_tokens: int) -> int:

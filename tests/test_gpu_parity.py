@@ -232,6 +232,22 @@ def test_wide_hidden(fmt, H):
     G.assert_close(G.out_f64(G.run_gpu(case)), G.oracle_out(case), fmt, f"H={H}")
 
 
+@pytest.mark.parametrize("name", ["mxfp8_small", "nvfp4_shared_norm"])
+def test_pinned_host_io_matches_device_io(name):
+    """hidden, ids, weights, gamma and out in pinned host memory (read and written by the kernels over the
+    host link) give the same bits as device buffers."""
+    shape = REDUCED[name]
+    run = G.run_gpu(G.float_case(shape))
+    pin = lambda t: None if t is None else t.cpu().pin_memory()
+    h = {k: pin(run.inputs[k]) for k in ("hidden", "topk_ids", "topk_weights", "gamma")}
+    out = torch.zeros(run.out.shape, dtype=run.out.dtype).pin_memory()
+    run.plan.forward(h["hidden"], h["topk_ids"], h["topk_weights"], run.kweights, l2_act_scale=run.inputs["a2"],
+                     shared=run.kshared, norm_gamma=h["gamma"], out=out, workspace=run.workspace)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), run.out.view(torch.int16).cpu())
+    assert run.plan.last_status(run.workspace) == 0
+
+
 def test_masked_slots_and_duplicates():
     shape = _small_case("mxfp8", T=96, k=3)
     ids, w = S.router(shape)
