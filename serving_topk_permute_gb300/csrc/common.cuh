@@ -63,14 +63,6 @@ __host__ __device__ inline int64_t act_sf_offset(int64_t r, int64_t kb, int S, i
 // one K stage of any 128- or 256-row tile are one contiguous run.
 __host__ __device__ inline int64_t wt_sf_blocks(int64_t N) { return (N + BN_MAX - 1) / BN_MAX * (BN_MAX / NBLK); }
 
-// Byte offset of scale block kb of kernel-layout weight row n of expert e.
-__host__ __device__ inline int64_t wt_sf_offset(int64_t e, int64_t n, int64_t kb, int S, int64_t nks,
-                                                int64_t n_blocks) {
-    const int64_t nb = n / NBLK, m = n % NBLK;
-    const int64_t ks = kb / (4 * S), s = (kb / 4) % S, b = kb % 4;
-    return ((((e * nks + ks) * n_blocks + nb) * S + s)) * ATOM_BYTES + (m % 32) * 16 + (m / 32) * 4 + b;
-}
-
 // w13 gate/up interleave: kernel row 128 b + 64 h + r (h 0 = gate, 1 = up, r < 64)
 // holds checkpoint row h * I + 64 b + r.
 __host__ __device__ inline int64_t w13_src_row(int64_t n, int64_t I) {
