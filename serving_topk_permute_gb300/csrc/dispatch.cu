@@ -4,9 +4,9 @@
 // per token; vllm.model_executor.layers.fused_moe, DeepGemmExperts.apply:
 // deepgemm_moe_permute writes a1q_perm).
 //
-// One CTA of 256 threads per token. Each thread owns 8-element chunks
-// c = tid + 256 i of the row (at most 4 of them for H <= 8192, 8 above), loaded as
-// one 128-bit bf16x8 vector each, kept in registers. Per format:
+// One CTA per token: 128 threads for H <= 4096 and T >= 1024, else 256. Each thread owns 8-element
+// chunks c = tid + NT i of the row (NT threads; at most 4 of them for H <= 8192, 8
+// above), loaded as one 128-bit bf16x8 vector each, kept in registers. Per format:
 //   BF16   the 16-byte chunk is copied as is
 //   MXFP8  a 32-element block is 4 neighbouring threads: block amax by two xor
 //          shuffles, e = smallest integer with amax <= 448 * 2^e, codes
@@ -32,6 +32,12 @@ constexpr int DISPATCH_MAX_CHUNKS = 8;   // H <= 8 * 256 * 8 = 16384
 // registers, so that 5 CTAs (tokens) are resident per SM instead of 3.
 constexpr int DISPATCH_SMALL_CHUNKS = 4;
 constexpr int DISPATCH_SMALL_MIN_CTAS = 5;
+// Rows of H <= 4096 in batches too large to be resident at once use CTAs of 128 threads
+// (4 chunks each), twice as many tokens in flight per SM. Smaller batches keep 256 threads:
+// there every CTA is resident anyway, and a narrower CTA only lengthens each thread's work.
+constexpr int DISPATCH_NARROW_THREADS = 128;
+constexpr int DISPATCH_NARROW_MIN_CTAS = 10;
+constexpr int DISPATCH_NARROW_MIN_TOKENS = 1024;
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -66,14 +72,14 @@ __device__ __forceinline__ int mxfp8_block_exponent(const float (&f)[8]) {
 
 // One token (routed layout: written to its k permuted rows) or one row of the batched
 // layout (batched: written to the same row).
-template <int MAXC>
+template <int MAXC, int NT>
 __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t, const bool batched) {
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     const int nchunks = a.H / 8;
     __shared__ int s_rows[32];
     __shared__ int s_rank[32];  // rank of slot j among the equal ids before it in its routing chunk
     __shared__ int s_exp[32];
-    __shared__ float s_amax[DISPATCH_THREADS / 32];
+    __shared__ float s_amax[NT / 32];
 
     // The token's row and its own scale do not depend on routing. The hidden states are
     // complete before this kernel starts (routing, the kernel before it, lets it start only
@@ -83,7 +89,7 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
     const uint4* xrow = reinterpret_cast<const uint4*>(a.x + (int64_t)t * a.H);
 #pragma unroll
     for (int i = 0; i < MAXC; ++i) {
-        const int c = tid + i * DISPATCH_THREADS;
+        const int c = tid + i * NT;
         v[i] = c < nchunks ? __ldcg(xrow + c) : make_uint4(0, 0, 0, 0);  // from L2: no stale L1 line
     }
 
@@ -102,11 +108,11 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
         s_rank[tid] = 0;
     }
     __syncthreads();
-    for (int base = c0; base < s0; base += 8 * DISPATCH_THREADS) {
+    for (int base = c0; base < s0; base += 8 * NT) {
         int v[8];
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-            const int i0 = base + 4 * tid + 4 * DISPATCH_THREADS * m;
+            const int i0 = base + 4 * tid + 4 * NT * m;
             if (i0 + 3 < s0) {
                 const int4 q = __ldcg(reinterpret_cast<const int4*>(a.ids + i0));
                 v[4 * m] = q.x, v[4 * m + 1] = q.y, v[4 * m + 2] = q.z, v[4 * m + 3] = q.w;
@@ -150,7 +156,7 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
         __syncthreads();
         amax = s_amax[0];
 #pragma unroll
-        for (int w = 1; w < DISPATCH_THREADS / 32; ++w) amax = fmaxf(amax, s_amax[w]);
+        for (int w = 1; w < NT / 32; ++w) amax = fmaxf(amax, s_amax[w]);
         gs = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
     }
     grid_dep_wait();  // routing has written the chunk bases (and the previous forward is done with x_scale)
@@ -171,8 +177,8 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
 
 #pragma unroll
     for (int i = 0; i < MAXC; ++i) {
-        const int c = tid + i * DISPATCH_THREADS;
-        if (i * DISPATCH_THREADS >= nchunks) break;  // uniform across the CTA
+        const int c = tid + i * NT;
+        if (i * NT >= nchunks) break;  // uniform across the CTA
         const bool in = c < nchunks;
         float f[8];
         bf16x8_to_f32(v[i], f);
@@ -250,10 +256,10 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
     if (batched) __syncthreads();  // the next row reuses the shared arrays
 }
 
-template <int MAXC, int MIN_CTAS>
-__global__ void __launch_bounds__(DISPATCH_THREADS, MIN_CTAS) dispatch_kernel(const DispatchArgs a) {
+template <int MAXC, int NT, int MIN_CTAS>
+__global__ void __launch_bounds__(NT, MIN_CTAS) dispatch_kernel(const DispatchArgs a) {
     if (!a.batch_counts) {
-        dispatch_one<MAXC>(a, blockIdx.x, false);
+        dispatch_one<MAXC, NT>(a, blockIdx.x, false);
         return;
     }
     // batched layout: the used rows, numbered 0 .. batch_prefix[E) in expert order, strided
@@ -271,17 +277,23 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, MIN_CTAS) dispatch_kernel(co
             else
                 hi = mid;
         }
-        dispatch_one<MAXC>(a, lo * a.batch_M + (i - a.batch_prefix[lo]), true);
+        dispatch_one<MAXC, NT>(a, lo * a.batch_M + (i - a.batch_prefix[lo]), true);
     }
 }
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl) {
     LaunchAttrs at(pdl);
     const int grid = a.batch_counts ? (a.T < 2048 ? a.T : 2048) : a.T;
+    if (a.H <= DISPATCH_SMALL_CHUNKS * DISPATCH_NARROW_THREADS * 8 && grid >= DISPATCH_NARROW_MIN_TOKENS) {
+        cudaLaunchConfig_t cfg = at.config(dim3(grid), dim3(DISPATCH_NARROW_THREADS), 0, st);
+        return cudaLaunchKernelEx(
+            &cfg, dispatch_kernel<DISPATCH_SMALL_CHUNKS, DISPATCH_NARROW_THREADS, DISPATCH_NARROW_MIN_CTAS>, a);
+    }
     cudaLaunchConfig_t cfg = at.config(dim3(grid), dim3(DISPATCH_THREADS), 0, st);
     if (a.H <= DISPATCH_SMALL_CHUNKS * DISPATCH_THREADS * 8)
-        return cudaLaunchKernelEx(&cfg, dispatch_kernel<DISPATCH_SMALL_CHUNKS, DISPATCH_SMALL_MIN_CTAS>, a);
-    return cudaLaunchKernelEx(&cfg, dispatch_kernel<DISPATCH_MAX_CHUNKS, 3>, a);
+        return cudaLaunchKernelEx(&cfg, dispatch_kernel<DISPATCH_SMALL_CHUNKS, DISPATCH_THREADS, DISPATCH_SMALL_MIN_CTAS>,
+                                  a);
+    return cudaLaunchKernelEx(&cfg, dispatch_kernel<DISPATCH_MAX_CHUNKS, DISPATCH_THREADS, 3>, a);
 }
 
 }  // namespace moe
