@@ -44,8 +44,8 @@ SF_PER_ELEM = {"bf16": 0.0, "mxfp8": 1.0 / 32, "nvfp4": 1.0 / 16, "mxfp4": 1.0 /
 # (profiles/grouped_gemm_*.md); an entry must be removed when its kernel changes. The
 # nvfp4_decode entries come from a capture at E=64 scaled by touched experts (249 / 64).
 NCU_TRAFFIC = {
-    ("mxfp8_small", "mlp"): (324.285952e6 + 7.355648e6, "profiles/fused_mlp_mxfp8_small.md"),
-    ("nvfp4_decode", "mlp"): ((1.600966e9 + 15.757056e6) * 249 / 64,
+    ("mxfp8_small", "mlp"): (324.157440e6 + 6.805504e6, "profiles/fused_mlp_mxfp8_small.md"),
+    ("nvfp4_decode", "mlp"): ((1.600900e9 + 16.153344e6) * 249 / 64,
                               "profiles/fused_mlp_nvfp4_decode_e64.md (E=64, scaled by 249/64 touched experts)"),
 }
 # tokens of one reference-arm step, and of the first (sizing) call of cpu_baseline
