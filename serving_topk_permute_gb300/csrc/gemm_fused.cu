@@ -4,13 +4,15 @@
 // launch, vllm.model_executor.layers.fused_moe.deep_gemm_mega_moe, module docstring).
 //
 // The tile list is every L1 tile (row tile x 256 w13 rows) followed by every L2 tile
-// (row tile x 256 w2 rows). CTAs take tiles in that order from a global counter, so
-// the CTAs that finish their L1 work early start L2 tiles while others are still on
-// their last L1 tile: the second GEMM has no ramp-up of its own and the first no
-// half-empty last round.
+// (row tile x 256 w2 rows), the row tiles of each phase in the order interleave_tile
+// gives (both ends of the expert order, see there). CTAs take tiles in that order
+// from a global counter, so the CTAs that finish their L1 work early start L2 tiles
+// while others are still on their last L1 tile: the second GEMM has no ramp-up of its
+// own and the first no half-empty last round. A row tile with at most 96 used rows
+// loads only the 32-row boxes of A that hold them.
 //
-// An L2 tile of row tile mt reads the L2 input (h codes and scale atoms) of rows
-// [128 mt, 128 mt + 128), which the epilogues of all L1 tiles of mt write. Each
+// An L2 tile of row tile mt reads the L2 input (h codes and scale atoms) of the
+// tile's 128 rows, which the epilogues of all L1 tiles of mt write. Each
 // epilogue warp publishes its part with a release increment of done[mt] (after a
 // fence and a proxy fence), and the producer of an L2 tile waits (bounded) until
 // done[mt] counts every warp of every L1 tile of mt, then issues a proxy fence
