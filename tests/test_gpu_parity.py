@@ -418,6 +418,26 @@ def test_batched_layout_matches_oracle(fmt):
     assert np.all(got[~used] == 7.0)
 
 
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_sparse_row_tile_box_boundaries(fmt):
+    """The one-kernel GEMM loads a row tile with at most 96 used rows in 32-row boxes and a fuller
+    one whole: used-row counts on each side of every box boundary (batched layout, one tile each)."""
+    E, M = 9, 128
+    case, xb, plan, kw, a2 = _batched_case(fmt, E, M)
+    counts = np.array([31, 32, 33, 64, 65, 96, 97, 127, 128], np.int32)
+    out = torch.full((E, M, xb.shape[2]), 7.0, dtype=torch.bfloat16, device=G.dev())
+    ws = torch.zeros(plan.batched_workspace_size(M), dtype=torch.uint8, device=G.dev())
+    plan.forward_batched(G.bf16_dev(xb.reshape(E * M, -1)).view(E, M, -1), G.to_dev(counts), kw, l2_act_scale=a2,
+                         out=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert plan.last_status(ws) == 0
+    want = OM.forward_batched(case.layer, xb, counts, exact=True)
+    got = out.float().cpu().numpy().astype(np.float64)
+    used = np.arange(M)[None, :] < counts[:, None]
+    G.assert_close(got[used], want[used], fmt, "box boundaries")
+    assert np.all(got[~used] == 7.0)
+
+
 def test_batched_layout_errors():
     """max_tokens not a multiple of 128 is refused; a count above max_tokens is clamped and
     reported as MOE_ERR_CAPACITY; a plan on CTA pairs cannot run the batched layout."""
