@@ -60,3 +60,33 @@ def test_algorithmic_work_counts_touched_experts():
     assert w["flops"] == 2.0 * R * 3 * shape.I * shape.H
     per_expert = 3 * shape.I * shape.H * (1 + 1 / 32)
     assert w["bytes"] == pytest.approx(shape.k * per_expert + 2 * shape.T * shape.H * 2)
+
+
+def test_roofline_picks_the_binding_resource_and_peak():
+    """An HBM-bound kernel is held against copy bandwidth, a tensor-bound one against the format's
+    tensor peak (the sustained bf16 figure x the nominal ratio when the power cap acted)."""
+    import bench
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1500.0}
+    work = {"per_kernel": {"mem": {"fmt": "mxfp8", "bytes": 6e9, "flops": 1e12},
+                           "mma": {"fmt": "mxfp8", "bytes": 1e9, "flops": 6e15}}}
+    r = bench.roofline("mem", work, 2.0, peaks, "measured", sustained=False)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6000.0
+    assert abs(r["achieved"] - 3000.0) < 1e-6 and abs(r["frac"] - 0.5) < 1e-9
+    r = bench.roofline("mma", work, 2000.0, peaks, "measured", sustained=True)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["peak"] == 1500.0 * bench.TENSOR_RATIO["mxfp8"]
+    assert abs(r["achieved"] - 3000.0) < 1e-6 and abs(r["frac"] - 3000.0 / r["peak"]) < 1e-6
+    r = bench.roofline("mma", work, 2000.0, peaks, "measured", sustained=False)
+    assert r["peak"] == 2000.0 * bench.TENSOR_RATIO["mxfp8"]
+
+
+def test_binding_accepts_host_memory_only_where_documented():
+    """Device tensors everywhere; a CPU tensor is refused unless pinned and the argument allows it."""
+    import torch
+    from serving_topk_permute_gb300 import moe as M
+    t = torch.zeros(4)
+    with pytest.raises(ValueError):
+        M._ptr(t)
+    with pytest.raises(ValueError):
+        M._ptr(t, host_ok=True)   # not pinned
+    assert M._ptr(None) is None
