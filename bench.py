@@ -41,12 +41,16 @@ TENSOR_RATIO = {"bf16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0, "mxfp4": 6.0}
 ELEM_BYTES = {"bf16": 2.0, "mxfp8": 1.0, "nvfp4": 0.5, "mxfp4": 0.5}
 SF_PER_ELEM = {"bf16": 0.0, "mxfp8": 1.0 / 32, "nvfp4": 1.0 / 16, "mxfp4": 1.0 / 32}
 # DRAM bytes (read + write) per launch from one ncu capture of the current kernels
-# (profiles/grouped_gemm_*.md); an entry must be removed when its kernel changes. The
-# nvfp4_decode entries come from a capture at E=64 scaled by touched experts (249 / 64).
+# (profiles/fused_mlp_*.md); an entry must be removed when its kernel changes. The
+# nvfp4_decode entries come from a capture at E=64 scaled by touched experts (249 / 64),
+# nvfp4_shared_norm from one at T=1024 E=32 (the same rows per expert) scaled 4x.
 NCU_TRAFFIC = {
     ("mxfp8_small", "mlp"): (324.157440e6 + 6.805504e6, "profiles/fused_mlp_mxfp8_small.md"),
     ("nvfp4_decode", "mlp"): ((1.600900e9 + 16.153344e6) * 249 / 64,
                               "profiles/fused_mlp_nvfp4_decode_e64.md (E=64, scaled by 249/64 touched experts)"),
+    ("nvfp4_shared_norm", "mlp"): ((368.400896e6 + 40.047872e6) * 4,
+                                   "profiles/fused_mlp_nvfp4_shared_norm_t1024_e32.md (T=1024 E=32, scaled 4x: "
+                                   "4x the experts and 4x the rows)"),
 }
 # tokens of one reference-arm step, and of the first (sizing) call of cpu_baseline
 CPU_SAMPLE_TOKENS = {"bf16_toy": 64, "mxfp8_small": 24, "nvfp4_decode": 3, "mxfp8_prefill_zipf": 12,
