@@ -270,6 +270,9 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+REFERENCE_BUDGET_S = 150.0   # host seconds the reference arm's timed steps may take in all
+
+
 def run_reference(args, shape: S.MoeShape):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -278,6 +281,10 @@ def run_reference(args, shape: S.MoeShape):
     smp = OracleSample(shape)
     for _ in range(args.warmup):
         smp.time(1)
+    # A step's sample: the first n_tok tokens, halved (down to one token) until the K timed steps
+    # fit the budget, so that the run ends within a few minutes whatever K is.
+    while n_tok > 1 and smp.time(n_tok) * args.steps > REFERENCE_BUDGET_S:
+        n_tok //= 2
     total_s, total_tok, cores = 0.0, 0, blas_threads()
     for i in range(args.steps):
         total_s += smp.time(n_tok)
