@@ -314,19 +314,22 @@ int moe_plan_kernel_times(moe_plan_t plan, float* ms, int32_t count);
  * The routing permutation of moe_forward (per-expert counts, BLOCK_M = 128
  * padded segment offsets, stable scatter) for callers that must not allocate
  * device memory: a runtime that owns all of HBM through its own pools, or a
- * path where a cudaMalloc is not allowed. The paper has no counterpart of this
+ * path where a cudaMalloc is not allowed. The pages have no counterpart of this
  * entry point; it exists for such callers only.
  *
  *   topk_ids        device int32 [T, k], -1 masks a slot (ids outside [-1, E)
- *                   are treated as masked)
+ *                   are treated as masked, and no status reports them: the
+ *                   kernel's error word stays in the private array)
  *   inv_perm        device int32 [T, k] (output): padded row of each slot, -1 if masked
  *   expert_offsets  device int32 [E + 1] (output): segment starts, [E] = padded total
  * Scratch lives in a fixed device array inside libmoe.so (about 1.06 MB per
  * GPU, held until the process exits): T * k + E * 127 must be <= 262144
  * (else MOE_ERR_CAPACITY, nothing launched); 1 <= k <= 32, 1 <= E <= 512.
  * The first call on a device sets that device up (looks up the array's
- * address); make it before any stream capture. Calls share the array: calls
- * whose GPU work overlaps race. Allocates nothing.
+ * address); make it before any stream capture. That set-up belongs to the
+ * CUDA context it was made in: do not call this again after a
+ * cudaDeviceReset in the same process. Calls share the array: calls whose GPU
+ * work overlaps race. Allocates nothing.
  */
 int moe_permute_noalloc(const int32_t* topk_ids, int32_t num_tokens, int32_t top_k, int32_t num_experts,
                         int32_t* inv_perm, int32_t* expert_offsets, void* stream);

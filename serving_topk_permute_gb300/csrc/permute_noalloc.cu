@@ -22,8 +22,14 @@
 //     capture.
 //   - All calls share the one array and it keeps the previous call's contents:
 //     calls whose GPU work overlaps (different streams without ordering
-//     between them) race on it. The parts that must start at zero are cleared
-//     by each call on its own stream.
+//     between them) race on it. The kernel itself clears what must start at
+//     zero (the error word) and writes every other word before reading it.
+//   - Ids outside [-1, E) are treated as masked. The kernel's error word stays
+//     in the private array and no call reads it back, so such ids produce no
+//     status; moe_forward reports them through moe_last_status.
+//   - The cached set-up belongs to the CUDA context it was made in: after a
+//     cudaDeviceReset the array's address and the kernel attribute are stale,
+//     so the entry point must not be used again in that process.
 //   - Nothing here allocates: no cudaMalloc, no cudaFree, no allocating
 //     library routine.
 #include <mutex>
@@ -76,8 +82,7 @@ extern "C" int moe_permute_noalloc(const int32_t* topk_ids, int32_t num_tokens, 
     const int rc = setup_device(dev, &s);
     if (rc != MOE_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // the error word must start at zero; everything else the kernel reads it writes first
-    if (cudaMemsetAsync(s + OFF_ERR, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    // the routing kernel zeroes the error word and writes every other word it reads first
     if (moe::launch_route(topk_ids, num_tokens, top_k, num_experts, moe::BM, s + OFF_CNT, expert_offsets, s + OFF_SRC,
                           inv_perm, s + OFF_TILES, s + OFF_META, s + OFF_ERR, st) != cudaSuccess)
         return MOE_ERR_CUDA;

@@ -124,15 +124,38 @@ def permute_noalloc(topk_ids: torch.Tensor, num_experts: int, inv_perm: torch.Te
                     expert_offsets: torch.Tensor | None = None, stream=None):
     """moe_permute_noalloc: the routing permutation with the library's fixed scratch array
     (for callers that must not allocate device memory; the output tensors are the
-    caller's). Returns (inv_perm int32 [T, k], expert_offsets int32 [E + 1])."""
+    caller's). Returns (inv_perm int32 [T, k], expert_offsets int32 [E + 1]).
+
+    The kernel reads and writes raw int32 buffers, so the tensors are checked here:
+    int32, contiguous, on one CUDA device, topk_ids 2-D, inv_perm of shape [T, k] and
+    expert_offsets with at least E + 1 elements. The call runs with that device
+    current, on its current stream unless `stream` is given."""
+    if not isinstance(topk_ids, torch.Tensor) or topk_ids.dim() != 2:
+        raise ValueError("topk_ids must be a 2-D tensor [T, k]")
+    if not topk_ids.is_cuda:
+        raise ValueError("topk_ids must be a CUDA tensor")
+    dev = topk_ids.device
     T, k = topk_ids.shape
     if inv_perm is None:
-        inv_perm = torch.empty((T, k), dtype=torch.int32, device=topk_ids.device)
+        inv_perm = torch.empty((T, k), dtype=torch.int32, device=dev)
     if expert_offsets is None:
-        expert_offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=topk_ids.device)
-    _check("moe_permute_noalloc", lib().moe_permute_noalloc(
-        _ptr(topk_ids) if T else None, T, k, num_experts, _ptr(inv_perm) if T else None, _ptr(expert_offsets),
-        _stream(stream)))
+        expert_offsets = torch.empty(max(num_experts, 0) + 1, dtype=torch.int32, device=dev)
+    for name, t in (("topk_ids", topk_ids), ("inv_perm", inv_perm), ("expert_offsets", expert_offsets)):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{name} must be int32, got {t.dtype}")
+        if not t.is_cuda or t.device != dev:
+            raise ValueError(f"{name} must be on {dev}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if tuple(inv_perm.shape) != (T, k):
+        raise ValueError(f"inv_perm must have shape {(T, k)}, got {tuple(inv_perm.shape)}")
+    if expert_offsets.numel() < num_experts + 1:
+        raise ValueError(f"expert_offsets needs at least {num_experts + 1} elements")
+    with torch.cuda.device(dev):
+        st = torch.cuda.current_stream(dev) if stream is None else stream
+        _check("moe_permute_noalloc", lib().moe_permute_noalloc(
+            topk_ids.data_ptr() if T else None, T, k, num_experts, inv_perm.data_ptr() if T else None,
+            expert_offsets.data_ptr(), st.cuda_stream))
     return inv_perm, expert_offsets
 
 

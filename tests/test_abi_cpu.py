@@ -91,3 +91,13 @@ def test_error_strings(pkg):
     for s in range(1, 8):
         assert pkg.error_string(s) and pkg.error_string(s) != "unknown status"
     assert pkg.error_string(99) == "unknown status"
+
+
+def test_noalloc_binding_refuses_host_tensors(pkg):
+    """moe_permute_noalloc reads raw device buffers: the binding refuses host or 1-D ids
+    before anything reaches the library."""
+    import torch
+    with pytest.raises(ValueError):
+        pkg.permute_noalloc(torch.zeros((4, 2), dtype=torch.int32), 8)
+    with pytest.raises(ValueError):
+        pkg.permute_noalloc(torch.zeros(8, dtype=torch.int32), 8)
