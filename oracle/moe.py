@@ -233,25 +233,55 @@ def forward(layer: Layer, x_bits, topk_ids, topk_weights, tokens=None, block_m: 
             for r, hh in zip(rows, h):
                 h_rows[r] = hh
 
-    z = np.zeros((len(toks), H), dtype=np.float64)
-    for i in range(len(toks)):
+    z = _combine_shared_norm(layer, x_bits[toks], w[toks], inv, y_rows)
+    out = F.bf16_bits(z)
+    if return_parts:
+        return out, dict(z=z, dispatched=disp, off=off, src=src, inv=inv, h=h_rows, y=y_rows)
+    return out
+
+
+def _combine_shared_norm(layer: Layer, x_bits_sub, w_sub, inv, y_rows) -> np.ndarray:
+    """z[i] = sum over j (ascending) of w[i, j] * y[inv[i, j]] (masked slots add nothing), plus the
+    shared expert, then the post-norm: the layer's value before its final bf16 rounding (fp64)."""
+    H = y_rows.shape[1]
+    n, k = inv.shape
+    z = np.zeros((n, H), dtype=np.float64)
+    for i in range(n):
         for j in range(k):
             r = inv[i, j]
             if r >= 0:
-                z[i] += w[toks[i], j] * y_rows[r]
-
+                z[i] += w_sub[i, j] * y_rows[r]
     if layer.shared is not None:
-        sd = dispatch_quantize(x_bits[toks], layer.shared.fmt)
+        sd = dispatch_quantize(x_bits_sub, layer.shared.fmt)
         z += expert_mlp(sd.x, layer.shared.w13_of(0), layer.shared.w2_of(0),
                         layer.shared.fmt, Activation())
     if layer.norm_gamma is not None:
         gamma = np.asarray(layer.norm_gamma, dtype=np.float32).astype(np.float64)
         rms = np.sqrt(np.mean(z * z, axis=1, keepdims=True) + layer.norm_eps)
         z = z / rms * gamma[None, :]
-    out = F.bf16_bits(z)
-    if return_parts:
-        return out, dict(z=z, dispatched=disp, off=off, src=src, inv=inv, h=h_rows, y=y_rows)
-    return out
+    return z
+
+
+def forward_from_l2_inputs(layer: Layer, x_bits, topk_ids, topk_weights, token: int, l2_inputs) -> np.ndarray:
+    """The layer's value before its final bf16 rounding (fp64) for one token, continuing from given
+    dequantised L2 inputs: ``l2_inputs[j]`` is slot j's requantised h (fp64 [I]; ignored for masked
+    slots). The same L2 GEMM, combine, shared expert and norm as ``forward``; used where a rounding
+    decision of the L2-input quantiser is a tie within fp32 accumulation noise, so that either
+    neighbouring code is a correct result."""
+    ids = np.asarray(topk_ids)
+    w = np.asarray(topk_weights, dtype=np.float32).astype(np.float64)
+    k = ids.shape[1]
+    H = layer.routed.w2.shape[1]
+    y_rows = np.zeros((k, H), dtype=np.float64)
+    inv = np.full((1, k), -1, dtype=np.int64)
+    for j in range(k):
+        e = int(ids[token, j])
+        if e < 0:
+            continue
+        y_rows[j] = np.asarray(l2_inputs[j], dtype=np.float64) @ layer.routed.w2_of(e).T
+        inv[0, j] = j
+    x_bits = np.asarray(x_bits)
+    return _combine_shared_norm(layer, x_bits[[token]], w[[token]], inv, y_rows)[0]
 
 
 def forward_batched(layer: Layer, x_bits, expert_num_tokens, exact: bool = False) -> np.ndarray:

@@ -175,6 +175,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
             for (int s = 0; s < STAGES; ++s) last_parity[s] = -1;
             int next = first;
+            // A full row tile belongs to an expert with many rows, whose weight tiles the
+            // expert's other row tiles read again: keep them in L2. A mostly empty one is
+            // (nearly always) an expert's only row tile, whose weights are read once: let them
+            // go first, so they do not push the reused weights out. (Measured on the
+            // Zipf-routed prefill shape: 1% faster than the default policy for both.)
+            const uint64_t pol_reused = make_policy_evict_last(), pol_once = make_policy_evict_first();
             for (int k = 0;; ++k) {
                 const int t = next;
                 const int r = k % TRING;
@@ -230,7 +236,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         for (int b = 0; b < a_boxes; ++b)
                             tma_load_2d(st + b * (A_BOX_ROWS * BK_BYTES), tmAs, full, ks * BK_BYTES,
                                         row0 + b * A_BOX_ROWS);
-                    tma_load_3d(st + C::A_BYTES, tmB, full, ks * BK_BYTES, nt * BN, e);
+                    tma_load_3d_hint(st + C::A_BYTES, tmB, full, ks * BK_BYTES, nt * BN, e,
+                                     whole ? pol_reused : pol_once);
                     if constexpr (S > 0) {
                         bulk_load(st + C::A_BYTES + C::B_BYTES,
                                   p.sfa + ((int64_t)(row0 / BM) * p.nks + ks) * C::SFA_BYTES, C::SFA_BYTES, full);

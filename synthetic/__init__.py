@@ -167,9 +167,9 @@ def shared_float_weights(shape: MoeShape, seed: int = 0):
 def mxfp8_codes(rows: int, K: int, seed: int, stream: int, index: int = 0):
     """E4M3 codes (any finite byte, both signs) [rows, K] and UE8M0 bytes [rows, K/32]."""
     g = _rng(seed, stream, index)
-    mag = g.integers(0x30, 0x7F, size=(rows, K), dtype=np.uint8)      # 0x30..0x7E: 1.0 .. 448
-    sign = (g.integers(0, 2, size=(rows, K), dtype=np.uint8) << 7).astype(np.uint8)
-    codes = (mag | sign).astype(np.uint8)
+    # one draw per code: 79 magnitudes 0x30..0x7E (1.0 .. 448) times 2 signs
+    v = g.integers(0, 158, size=(rows, K), dtype=np.uint16)
+    codes = ((0x30 + v % 79) | ((v >= 79).astype(np.uint16) << 7)).astype(np.uint8)
     centre = 127 + int(round(-math.log2(96.0) - 0.5 * math.log2(K)))
     sf = g.integers(centre - 1, centre + 2, size=(rows, K // 32), dtype=np.int64).astype(np.uint8)
     return codes, sf
@@ -179,7 +179,7 @@ def mxfp4_codes(rows: int, K: int, seed: int, stream: int, index: int = 0):
     """Packed E2M1 bytes [rows, K/2] (every nibble equally likely, rms value 2.93) and
     UE8M0 bytes [rows, K/32] around 1 / (2.93 sqrt(K)): weights of rms about 1/sqrt(K)."""
     g = _rng(seed, stream, index)
-    codes = g.integers(0, 256, size=(rows, K // 2), dtype=np.uint16).astype(np.uint8)
+    codes = np.frombuffer(g.bytes(rows * (K // 2)), np.uint8).reshape(rows, K // 2).copy()
     centre = 127 + int(round(-math.log2(2.93) - 0.5 * math.log2(K)))
     sf = g.integers(centre - 1, centre + 2, size=(rows, K // 32), dtype=np.int64).astype(np.uint8)
     return codes, sf
@@ -188,7 +188,7 @@ def mxfp4_codes(rows: int, K: int, seed: int, stream: int, index: int = 0):
 def nvfp4_codes(rows: int, K: int, seed: int, stream: int, index: int = 0):
     """Packed E2M1 bytes [rows, K/2], E4M3 block-scale bytes [rows, K/16], fp32 global scale."""
     g = _rng(seed, stream, index)
-    codes = g.integers(0, 256, size=(rows, K // 2), dtype=np.uint16).astype(np.uint8)
+    codes = np.frombuffer(g.bytes(rows * (K // 2)), np.uint8).reshape(rows, K // 2).copy()
     sf = g.integers(0x38, 0x59, size=(rows, K // 16), dtype=np.uint16).astype(np.uint8)  # 1.0 .. 16
     gs = np.float32(1.0 / (12.0 * math.sqrt(K)) * g.uniform(0.8, 1.25))
     return codes, sf, gs

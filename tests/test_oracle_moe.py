@@ -210,3 +210,30 @@ def test_batched_layout_equals_routed_top1(fmt):
         assert np.array_equal(out_b[e, m], out_r[i]), (e, m)
     for e in range(4):
         assert not out_b[e, counts[e]:].any()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "bf16"])
+def test_forward_from_l2_inputs_reproduces_forward(fmt):
+    """Continuing from the oracle's own requantised L2 inputs gives the forward's value (shared
+    expert and norm included) up to fp64 summation order (one row at a time instead of a
+    matrix product), so the continuation adds nothing of its own."""
+    shape = S.shrink(S.WORKLOADS["nvfp4_shared_norm"], T=6, H=256, I=256, E=4, k=3, fmt=fmt, shared_I=256)
+    x = S.hidden_states(shape)
+    ids, w = S.router(shape)
+    ids = ids.copy()
+    ids[2, 1] = -1                                   # a masked slot
+    w13f, w2f = S.routed_float_weights(shape)
+    layer = M.Layer(shape.E, shape.k, M.quantize_weights(fmt, w13f, w2f))
+    if fmt == "nvfp4":
+        layer.a2 = M.calibrate_a2(layer, x, ids)
+    s13, s2 = S.shared_float_weights(shape)
+    layer.shared = M.quantize_weights("mxfp8", s13[None], s2[None])
+    layer.norm_gamma = S.norm_gamma(shape)
+    _, parts = M.forward(layer, x, ids, w, return_parts=True)
+    for t in range(shape.T):
+        l2 = []
+        for j in range(shape.k):
+            r = parts["inv"][t, j]
+            l2.append(None if r < 0 else M.l2_input_quantize(parts["h"][r][None], fmt, layer.a2)[0])
+        z = M.forward_from_l2_inputs(layer, x, ids, w, t, l2)
+        assert np.allclose(z, parts["z"][t], rtol=1e-12, atol=1e-12 * np.abs(parts["z"][t]).max())
