@@ -538,6 +538,56 @@ def run_ours(args, shape: S.MoeShape):
             e2e_value = zc_value
             transfer = ("no copy engine: the kernels read the inputs from, and write the output to, pinned host "
                         "memory over the host link")
+    ov_value = None
+    if not args.batched:
+        # the serving pattern: step i's inputs go over while step i-1 computes and step i-2's output
+        # comes back. Two device input buffers and two output buffers; a copy-in stream, the compute
+        # stream and a copy-out stream, chained by events. One timed region from the first input copy to
+        # the last output copy, so every step's copies lie inside it. No L2 flush between steps: the
+        # weights a step streams are larger than L2 (the workloads' touched weights are 0.16 to 8.6 GB).
+        s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        d_in2 = [d_stage, torch.empty_like(d_stage)]
+        x_in2 = [[d[off:off + arr.nbytes].view(torch_dt[arr.dtype]).view(arr.shape) for arr, off in zip(host_inputs, offs)]
+                 for d in d_in2]
+        y_dev2 = [torch.zeros_like(out), torch.zeros_like(out)]
+        y_host2 = [torch.empty(out.shape, dtype=torch.int16).pin_memory() for _ in range(2)]
+        ev_in = [torch.cuda.Event() for _ in range(args.steps)]
+        ev_comp = [torch.cuda.Event() for _ in range(args.steps)]
+        ev_out = [torch.cuda.Event() for _ in range(args.steps)]
+        ov_start, ov_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        ov_start.record(s_in)
+        for i in range(args.steps):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_comp[i - 2])      # forward i-2 has read this input buffer
+                d_in2[b].copy_(h_stage, non_blocking=True)
+                ev_in[i].record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(ev_in[i])
+                if i >= 2:
+                    s_comp.wait_event(ev_out[i - 2])     # output i-2 has left this output buffer
+                plan.forward(x_in2[b][0], x_in2[b][1], x_in2[b][2], kw, l2_act_scale=a2, shared=ks, norm_gamma=gamma,
+                             out=y_dev2[b], workspace=ws, stream=s_comp)
+                ev_comp[i].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[i])
+                y_host2[b].copy_(y_dev2[b].view(torch.int16), non_blocking=True)
+                ev_out[i].record(s_out)
+        ov_end.record(s_out)
+        torch.cuda.synchronize()
+        barrier()
+        assert torch.equal(y_host2[(args.steps - 1) % 2], out.view(torch.int16).cpu()), \
+            "overlapped end-to-end output differs from the graph's"
+        ov_ms = reduce_max(ov_start.elapsed_time(ov_end))
+        ov_value = world * T * args.steps / (ov_ms / 1e3)
+        if ov_value > e2e_value:
+            e2e_value = ov_value
+            transfer = ("copy engine, overlapped: each step's input copy and the previous step's output copy run "
+                        "beside the compute of the step between them (two buffers each, three streams); one timed "
+                        "region over all steps, no L2 flush (the weights streamed per step exceed L2)")
     h2d = sum(arr.nbytes for arr in host_inputs)
     d2h = h_out.numel() * 2
     if plan.last_status(ws) != 0:
@@ -592,7 +642,8 @@ def run_ours(args, shape: S.MoeShape):
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "transfer": transfer,
                 "copy_engine_value": round(copy_value, 1),
-                "zero_copy_value": round(zc_value, 1) if zc_value is not None else None},
+                "zero_copy_value": round(zc_value, 1) if zc_value is not None else None,
+                "overlapped_value": round(ov_value, 1) if ov_value is not None else None},
         "gpu_launches": len(avg_k) * args.steps,   # this library's kernels per forward (those the per-kernel timing saw run)
         "timing": "value: CUDA-graph replays of one moe_forward, events per step; e2e: plain C-ABI calls; "
                   "per-kernel: " + kernel_timing,
