@@ -613,7 +613,7 @@ def run_ours(args, shape: S.MoeShape):
     # the sustained (power-capped) tensor peak when the power cap acted during the timed steps, else the burst one
     rl = roofline(dominant, work, avg_k[dominant], peaks, source,
                   sustained="sw_power_cap" in (clk.get("reasons") or []))
-    rl["traffic"], rl["traffic_source"] = measured_traffic(shape.name, dominant)
+    rl["traffic"], rl["traffic_source"] = measured_traffic(shape.name + ("+batched" if args.batched else ""), dominant)
     rl["staging_bytes"] = {k_: int(v) for k_, v in work["staging_bytes"].items()}
     rl["kernel_ms"] = {k_: round(v, 4) for k_, v in avg_k.items()}
     sec = sum(step_ms) / 1e3 / args.steps
