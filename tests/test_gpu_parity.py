@@ -188,6 +188,30 @@ def test_forward_matches_oracle_full_size_sampled(name):
     G.assert_close_allowing_ties(run, case, sample, got, G.oracle_out(case, tokens=sample), name)
 
 
+_FULL_PREFILL = {}
+
+
+@pytest.mark.parametrize("mode", ["split256", "pair"])
+def test_prefill_full_size_other_gemm_modes(mode):
+    """The two-kernel GEMM and the CTA-pair GEMM (256-row segments) on the full Zipf-routed prefill
+    workload, on the same tile-covering token sample as the default mode (the oracle's values are
+    computed once for both)."""
+    import serving_topk_permute_gb300 as pkg
+    shape = W["mxfp8_prefill_zipf"]
+    if "case" not in _FULL_PREFILL:
+        probe = pkg.Plan(pkg.LayerConfig(shape.E, shape.H, shape.I, shape.k, shape.T, shape.fmt))
+        sample = _tile_covering_sample(shape, probe.block_m(shape.T))
+        del probe
+        case = G.code_case(shape, sample)
+        _FULL_PREFILL.update(case=case, sample=sample, want=G.oracle_out(case, tokens=sample))
+    case, sample, want = _FULL_PREFILL["case"], _FULL_PREFILL["sample"], _FULL_PREFILL["want"]
+    run = G.run_gpu(case, **G.MODES[mode])
+    if mode == "pair":
+        assert run.plan.block_m(shape.T) == 256
+    G.assert_close_allowing_ties(run, case, sample, G.out_f64(run)[sample], want, f"prefill {mode}")
+    assert run.plan.last_status(run.workspace) == 0
+
+
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
 def test_full_hidden_float_weights(fmt):
     """The full hidden and intermediate sizes (H = 7168, I = 2048: the whole 56-stage L1 and 16-stage L2 K
