@@ -645,7 +645,8 @@ def run_ours(args, shape: S.MoeShape):
                 "zero_copy_value": round(zc_value, 1) if zc_value is not None else None,
                 "overlapped_value": round(ov_value, 1) if ov_value is not None else None},
         "gpu_launches": len(avg_k) * args.steps,   # this library's kernels per forward (those the per-kernel timing saw run)
-        "timing": "value: CUDA-graph replays of one moe_forward, events per step; e2e: plain C-ABI calls; "
+        "timing": "value: CUDA-graph replays of one moe_forward, events per step; e2e: C-ABI calls with host "
+                  "I/O (copy engine and zero copy: events per step; overlapped: one region over all steps); "
                   "per-kernel: " + kernel_timing,
         "clocks": clk,
         "wall_s": round(wall, 3),
