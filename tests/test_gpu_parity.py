@@ -558,3 +558,34 @@ def test_bounded_wait_timeout_reports_and_context_survives(mode):
     torch.cuda.synchronize()
     assert run.plan.last_status(run.workspace) == 0
     assert np.array_equal(out.float().cpu().numpy(), good)
+
+
+# ----------------------------------------------------------------------------- seeded random shapes
+
+def _random_shape(i: int):
+    """Shape i of a seeded sweep over formats, sizes, expert counts, top-k, token counts (1 to 600),
+    routing skew, shared expert and norm: the tile, box and segment boundaries fall in many places."""
+    g = np.random.default_rng(9000 + i)
+    fmt = ["bf16", "mxfp8", "nvfp4", "mxfp4"][i % 4]
+    four_bit = fmt in ("nvfp4", "mxfp4")
+    H = int(g.choice([256, 512, 768] if four_bit else [256, 384, 512, 768]))
+    I = int(g.choice([256, 512] if four_bit else [128, 256, 384, 512]))
+    E = int(g.integers(1, 25))
+    k = int(g.integers(1, min(8, E) + 1))
+    T = int(g.choice([1, 2, 7, 31, 64, 129, 200, 333, 511, 600]))
+    shared = fmt == "nvfp4" and bool(g.integers(0, 2))
+    base = W["nvfp4_shared_norm"] if shared else W["mxfp8_prefill_zipf"]
+    return S.shrink(base, name=f"random{i}", T=T, H=H, I=I, E=E, k=k, fmt=fmt,
+                    zipf_s=float(g.choice([0.0, 1.1])), shared_I=256 if shared else 0, post_norm=shared)
+
+
+@pytest.mark.parametrize("i", range(36))
+def test_random_shapes_match_oracle(i):
+    """Every output element of each shape against the oracle, the GEMM mode rotating over the
+    one-kernel, two-kernel and CTA-pair variants."""
+    shape = _random_shape(i)
+    case = G.float_case(shape)
+    run = G.run_gpu(case, **G.MODES[["fused", "split256", "pair"][(i // 4) % 3]])
+    tokens = list(range(shape.T))
+    G.assert_close_allowing_ties(run, case, tokens, G.out_f64(run), G.oracle_out(case), shape.name)
+    assert run.plan.last_status(run.workspace) == 0
