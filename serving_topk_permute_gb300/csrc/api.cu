@@ -423,7 +423,7 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool p
                    const int* tile_expert, const int* src, int m_valid, const float* x_scale, const float* a2,
                    uint8_t* hq, uint8_t* hsf, float* h_debug, __nv_bfloat16* y, int* err, bool activation,
                    uint32_t* sched, cudaStream_t st, const BatchRows* br = nullptr,
-                   const int* seg_off = nullptr, const int* seg_cnt = nullptr) {
+                   const int* seg_off = nullptr, const int* seg_cnt = nullptr, bool independent = false) {
     const moe_config_t& c = p->cfg;
     const int S = fmt_sf_atoms(fmt);
     const int bn = pair ? 2 * BM : choose_bn(c, 0);
@@ -492,7 +492,7 @@ static int run_mlp(moe_plan_s* p, int kid1, int fmt, int E, int I, int H, bool p
         // the one-kernel GEMM loads mostly empty row tiles in smaller boxes
         if (!map_2d(&ta1s, xq, fmt_row_bytes(fmt, H), rows, A_BOX_ROWS)) return MOE_ERR_CUDA;
         if (!map_2d(&ta2s, hq, fmt_row_bytes(fmt, I), rows, A_BOX_ROWS)) return MOE_ERR_CUDA;
-        FusedSched fs{sched, sched + 1};
+        FusedSched fs{sched, sched + 1, independent && p->pdl ? 1 : 0};
         const int64_t tiles = m_tiles_max * (g1.n_tiles + g2.n_tiles);
         const int grid = (int)std::min<int64_t>(p->num_sms, std::max<int64_t>(1, tiles));
         KernelTimer kt(p, kid1, st);
@@ -592,7 +592,8 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
         const int tiles = (int)(L.t_pad / (shared_pair ? 2 * BM : BM));
         rc = run_mlp(plan, MOE_KERNEL_SHARED_L1, d.sfmt, 1, d.Is, d.H, shared_pair, R(R_SXQ), R(R_SXSF), L.t_pad, shared, nullptr, tiles, tiles, nullptr,
                      nullptr, T, nullptr, nullptr, R(R_SHQ), R(R_SHSF), nullptr, (__nv_bfloat16*)R(R_SY), err, false,
-                     (uint32_t*)R(R_SCHED) + 1 + L.m_tiles_max, st);
+                     (uint32_t*)R(R_SCHED) + 1 + L.m_tiles_max, st, nullptr, nullptr, nullptr,
+                     /*independent: reads only dispatch's shared-expert rows, never the routed GEMMs' output*/ true);
         if (rc != MOE_OK) return rc;
     }
     CombineArgs ca{};

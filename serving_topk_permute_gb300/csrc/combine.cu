@@ -45,9 +45,12 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 4) combine_kernel(const Combi
     __shared__ int s_rows[32];
     __shared__ float s_w[32];
     __shared__ float s_red[COMBINE_THREADS / 32];
-    // inv_perm (routing) and the weights (an input) are complete before this kernel starts:
-    // every kernel of the forward lets its successor start only after its own wait, so
-    // routing finished before the GEMM did its wait. y is read after the wait.
+    // inv_perm and the weights (an input) are complete before this kernel starts: it
+    // starts only after the GEMM launch before it has started, and that launch (or the
+    // routed GEMMs before the shared expert's) started only after the routed GEMMs' own
+    // wait for dispatch. y is read after the wait, which returns once the GEMM launch
+    // before this kernel has completed; a shared-expert launch completes only after the
+    // routed GEMMs have.
     if (tid < a.k) {
         s_rows[tid] = __ldcg(a.inv + (int64_t)t * a.k + tid);  // from L2: no stale L1 line
         s_w[tid] = __ldcg(a.w + (int64_t)t * a.k + tid);

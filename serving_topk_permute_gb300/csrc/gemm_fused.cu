@@ -133,8 +133,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     // What the routing kernel wrote (the row-tile count and experts, the zeroed tile
     // counter) is complete before this kernel starts, even while the kernel just before
-    // it (dispatch) still runs: every kernel of the forward lets its successor start
-    // only after its own grid-dependency wait, so by then routing has finished. So the
+    // it (dispatch, or the routed GEMMs before the shared expert) still runs: that kernel
+    // lets this one start only after its own grid-dependency wait, so by then routing
+    // (and, before the shared expert, dispatch) has finished. So the
     // producer takes its first tile and starts pulling that tile's first weight stages
     // into L2 before the wait, overlapping the previous kernel. (Loads bypass L1.)
     const int m_tiles = p1.m_tiles_dev ? __ldcg(p1.m_tiles_dev) : p1.m_tiles_host;
@@ -151,7 +152,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 tma_prefetch_3d(&tmB1, ks * BK_BYTES, nt * BN, e);
         }
     }
-    grid_dep_wait();  // everything below may read the previous kernel's output
+    // everything below may read the previous kernel's output; an independent launch reads
+    // none of it and waits for that kernel only at its end (a CTA of it becomes resident
+    // on an SM only once the previous kernel's CTA there has left, so it fills that
+    // kernel's tail)
+    if (!fs.independent) grid_dep_wait();
     grid_dep_launch();
 
     auto give_up = [&]() {
@@ -383,6 +388,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
+    // the successor's own wait covers this kernel only: this grid completes after the
+    // previous one
+    if (fs.independent) grid_dep_wait();
 }
 
 // ------------------------------------------------------------------ host side

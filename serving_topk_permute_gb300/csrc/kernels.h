@@ -132,6 +132,11 @@ cudaError_t gemm_prepare(int fmt);   // sets the dynamic shared memory attribute
 struct FusedSched {
     uint32_t* counter;
     uint32_t* done;
+    // 1: the kernel reads nothing the kernel launched just before it writes (the shared
+    // expert after the routed GEMMs). It then takes its tiles as soon as it is resident
+    // and waits for that kernel only before it exits, so its successor still finds both
+    // complete.
+    int independent;
 };
 cudaError_t fused_prepare(int fmt);
 cudaError_t launch_fused_mlp(int fmt, const CUtensorMap& a1, const CUtensorMap& b1, const CUtensorMap& a2,

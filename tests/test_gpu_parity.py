@@ -366,40 +366,48 @@ def test_deterministic(fmt, mode):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "nvfp4_shared_norm"])
 def test_back_to_back_forwards_overlapped_launch(fmt):
     """Forwards queued back to back on one workspace and stream, each kernel's set-up overlapping the
     previous kernel (the default launch), equal forwards run one at a time with serialised launches.
-    Forward n+1's routing rewrites inv_perm while forward n's combine may still be queued."""
+    Forward n+1's routing rewrites inv_perm while forward n's combine may still be queued. With a
+    shared expert, its GEMM launch takes SMs while the routed GEMMs are still finishing (it waits
+    for them only before it exits), and the combine must still see both."""
     import serving_topk_permute_gb300 as pkg
-    shape = _small_case(fmt, T=150, k=4, E=8)
+    if fmt == "nvfp4_shared_norm":
+        shape = S.shrink(W["nvfp4_shared_norm"], T=150, H=512, I=256, E=8, k=4, shared_I=512)
+    else:
+        shape = _small_case(fmt, T=150, k=4, E=8)
     case = G.float_case(shape)
     x2 = S.hidden_states(shape, 1)
     ids2, w2 = S.router(shape, 1)
     inputs = [(G.bf16_dev(case.x), G.to_dev(case.ids.astype(np.int32)), G.to_dev(case.w.astype(np.float32))),
               (G.bf16_dev(x2), G.to_dev(np.asarray(ids2, np.int32)), G.to_dev(np.asarray(w2, np.float32)))]
-    a2 = torch.tensor([np.float32(case.layer.a2)], device=G.dev()) if fmt == "nvfp4" else None
+    a2 = torch.tensor([np.float32(case.layer.a2)], device=G.dev()) if shape.fmt == "nvfp4" else None
+    gamma = None if case.layer.norm_gamma is None else G.to_dev(np.asarray(case.layer.norm_gamma, np.float32))
     outs = {}
     for serial in (True, False):
         cfg = G.layer_config(case)
         cfg.serial = serial
         plan = pkg.Plan(cfg)
         kw = plan.transform_weights(G._ckpt_dev(case.layer.routed))
+        ks = plan.transform_shared_weights(G._ckpt_dev(case.layer.shared)) if case.layer.shared else None
         ws = plan.alloc_workspace(shape.T)
         res = []
         for i in (0, 1, 0, 1):
             if serial:
                 torch.cuda.synchronize()
             h, ids, w = inputs[i]
-            res.append(plan.forward(h, ids, w, kw, l2_act_scale=a2, workspace=ws))
+            res.append(plan.forward(h, ids, w, kw, l2_act_scale=a2, shared=ks, norm_gamma=gamma, workspace=ws))
         torch.cuda.synchronize()
         assert plan.last_status(ws) == 0
         outs[serial] = [r.view(torch.int16) for r in res]
     for j in range(4):
         assert torch.equal(outs[True][j], outs[False][j]), f"forward {j}"
     assert torch.equal(outs[False][0], outs[False][2]) and torch.equal(outs[False][1], outs[False][3])
-    G.assert_close(outs[False][0].view(torch.bfloat16).float().cpu().numpy().astype(np.float64),
-                   G.oracle_out(case), fmt, "overlapped launch")
+    if case.layer.shared is not None:
+        G.assert_close(outs[False][0].view(torch.bfloat16).float().cpu().numpy().astype(np.float64),
+                       G.oracle_out(case), shape.fmt, "shared expert, overlapped launch")
 
 
 @pytest.mark.parametrize("alpha,beta,clamp", [(1.702, 1.0, 7.0), (1.0, 0.0, 0.5), (0.5, -0.25, None)])
