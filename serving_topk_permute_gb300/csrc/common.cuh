@@ -404,6 +404,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// four consecutive 32-bit columns of the 32 tensor-memory lanes of this warp's quarter:
+// lane i of the warp writes v to lane i of the quarter (taddr carries the quarter's first lane)
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint4& v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------------ clusters and 2-CTA (cta_group::2) MMA
 __device__ __forceinline__ uint32_t cluster_ctarank() {

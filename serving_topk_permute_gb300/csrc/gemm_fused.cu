@@ -20,13 +20,16 @@
 // CTAs have already taken from the counter, and those never wait on L2 tiles, so
 // the waits always end. The routing kernel zeroes the counter and done[] per forward.
 //
-// Per CTA (576 threads, one per SM), as in the two-kernel path:
+// Per CTA (one per SM; 576 threads, 704 for NVFP4):
 //   warp 0 lane 0  takes tile indices (one fetch ahead), hands each to the other
 //                  warps through a 4-entry ring in shared memory, and loads the
 //                  tile's A / B / scale-atom stages (TMA tiled + bulk copies)
 //   warp 1 lane 0  MMA issuer (tcgen05, 128 x 256 x 32 B per instruction)
 //   warps 2..17    epilogue: registers first, then the accumulator is released,
 //                  then SwiGLU + requant (L1) or the bf16 row store (L2)
+//   warps 18..21   NVFP4: each stage's scale factors, from shared memory into tensor
+//                  memory with tcgen05.st (one warp per lane quarter); the other formats'
+//                  MMA thread copies its 3 or 6 scale atoms per stage itself (tcgen05.cp)
 // Every wait is bounded; a CTA that gives up reports MOE_ERR_TIMEOUT and still waits
 // for its own copies and MMAs before freeing tensor memory.
 #include "gemm_epilogue.cuh"
@@ -49,12 +52,19 @@ struct FusedCfg {
     static constexpr int STAGE_BYTES = (TX_BYTES + 1023) / 1024 * 1024;
     static constexpr int ACC_COLS = BN;
     static constexpr int SF_COLS = 4 * S * (1 + NB);
+    // NVFP4 (12 scale-atom copies per stage): four more warps, one per tensor-memory lane
+    // quarter, write each stage's scale factors into tensor memory, so that the MMA thread
+    // issues only MMAs. (Measured: NVFP4 GEMMs 13% faster; with the 3 or 6 copies per stage
+    // of MXFP8 / MXFP4 it was 3-7% slower than the MMA thread's own copies, so those keep them.)
+    static constexpr int SF_WARPS = S == 4 ? 4 : 0;
+    static constexpr int THREADS = GEMM_THREADS + 32 * SF_WARPS;
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
     static_assert(ACC_COLS + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM <= 232448, "shared memory budget");
-    // barriers: full[STAGES], empty[STAGES], tfull, tempty, drain, tile_full[TRING], tile_empty[TRING]
-    static constexpr int NUM_BARS = 2 * STAGES + 3 + 2 * TRING;
+    // barriers: full[STAGES], empty[STAGES], tfull, tempty, drain, tile_full[TRING], tile_empty[TRING],
+    // sf_full[STAGES]
+    static constexpr int NUM_BARS = 3 * STAGES + 3 + 2 * TRING;
     static_assert(NUM_BARS * 8 + (TRING + 4) * 4 <= BAR_BYTES, "barrier area");
 };
 
@@ -75,7 +85,7 @@ __device__ __forceinline__ int interleave_tile(int i, int m) {
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(FusedCfg<FMT>::THREADS, 1)
     fused_mlp_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                      const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                      const __grid_constant__ CUtensorMap tmA1s, const __grid_constant__ CUtensorMap tmA2s,
@@ -98,6 +108,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t drain_bar = tfull_bar + 16;
     const uint32_t tile_full0 = tfull_bar + 24;
     const uint32_t tile_empty0 = tile_full0 + 8 * TRING;
+    const uint32_t sf_full0 = tile_empty0 + 8 * TRING;  // a stage's scale factors are in tensor memory
+    constexpr bool SFW = C::SF_WARPS > 0;
     const uint64_t tmo = p1.timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -110,8 +122,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         mbar_init(drain_bar, 1);
         for (int r = 0; r < TRING; ++r) {
             mbar_init(tile_full0 + 8 * r, 1);
-            mbar_init(tile_empty0 + 8 * r, 1 + EPI_WARPS);  // the MMA thread and every epilogue warp
+            mbar_init(tile_empty0 + 8 * r, 1 + EPI_WARPS + C::SF_WARPS);  // the MMA thread, the other warps
         }
+        for (int s = 0; s < STAGES; ++s) mbar_init(sf_full0 + 8 * s, SFW ? C::SF_WARPS : 1);
         *abort_flag = 0;
         *never = 0;
         fence_mbar_init();
@@ -296,7 +309,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     const uint32_t st = smem_u32(smem + stage * C::STAGE_BYTES);
                     const uint32_t sfa_col = tmem_base + C::ACC_COLS + stage * C::SF_COLS;
                     const uint32_t sfb_col = sfa_col + 4 * S;
-                    if constexpr (S > 0) {
+                    if constexpr (SFW) {
+                        // the scale-factor warps have written this stage's scale factors to tensor memory
+                        if (!mbar_wait(sf_full0 + 8 * stage, phase, tmo, abort_flag)) {
+                            give_up();
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    } else if constexpr (S > 0) {
                         const uint32_t sfa_smem = st + C::A_BYTES + C::B_BYTES;
 #pragma unroll
                         for (int a = 0; a < S; ++a) tc_cp_sf_atom(sfa_col + 4 * a, sf_atom_desc(sfa_smem + a * ATOM_BYTES));
@@ -338,7 +359,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tc_commit(drain_bar);
             mbar_wait(drain_bar, 0, DRAIN_TIMEOUT_NS, never);
         }
-    } else {
+    } else if (warp < 2 + EPI_WARPS) {
         const int q = warp % 4;           // the lane quarter of tensor memory this warp may read
         const int cg = (warp - 2) / 4;    // which quarter of the tile's columns it handles
         uint32_t acc_phase = 0;
@@ -382,6 +403,61 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             acc_phase ^= 1;
         }
+    } else if constexpr (SFW) {
+        // Scale-factor warps, one per lane quarter of tensor memory (warps 18..21: quarters
+        // 2, 3, 0, 1). For each stage, once it has landed, a warp stores the stage's scale
+        // atoms into its own quarter with tcgen05.st, in the layout a 32x128b.warpx4 copy of
+        // each atom gives: lane i, columns 4 a .. 4 a + 3 <- bytes 16 i .. 16 i + 15 of the
+        // atom copied to column 4 a. Then the MMA thread issues only MMAs. A stage's columns
+        // are written again only after its next fill has landed, which follows the commit
+        // of the MMAs that read them.
+        const int q = warp % 4;
+        const uint32_t quarter = tmem_base + ((uint32_t)(q * 32) << 16);
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int k = 0;; ++k) {
+            const int r = k % TRING;
+            if (!__all_sync(0xffffffffu, mbar_wait(tile_full0 + 8 * r, (k / TRING) & 1, tmo, abort_flag))) {
+                give_up();
+                break;
+            }
+            const int t = tile_slot[r];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tile_empty0 + 8 * r);
+            if (t < 0) break;
+            const int nks = t < total1 ? p1.nks : p2.nks;
+            bool ok = true;
+            for (int ks = 0; ks < nks; ++ks) {
+                if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * stage, phase, tmo, abort_flag))) {
+                    give_up();
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t* sf = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+                const uint32_t col = quarter + C::ACC_COLS + stage * C::SF_COLS;
+#pragma unroll
+                for (int a = 0; a < S; ++a)
+                    tmem_st4(col + 4 * a, *reinterpret_cast<const uint4*>(sf + a * ATOM_BYTES + 16 * lane));
+                // smem holds the weight atoms as [block][s]; tensor memory wants [s][block]
+#pragma unroll
+                for (int a = 0; a < S; ++a)
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb)
+                        tmem_st4(col + 4 * S + 4 * (a * NB + nb),
+                                 *reinterpret_cast<const uint4*>(sf + C::SFA_BYTES + (nb * S + a) * ATOM_BYTES +
+                                                                 16 * lane));
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sf_full0 + 8 * stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+        }
     }
     __syncthreads();
     if (warp == 1) {
@@ -414,7 +490,7 @@ static cudaError_t fused_t(const CUtensorMap& a1, const CUtensorMap& b1, const C
                            const CUtensorMap& b2, const CUtensorMap& a1s, const CUtensorMap& a2s, const GemmArgs& p1,
                            const GemmArgs& p2, const FusedSched& fs, int grid, cudaStream_t st, bool pdl) {
     LaunchAttrs at(pdl);
-    cudaLaunchConfig_t cfg = at.config(dim3(grid), dim3(GEMM_THREADS), FusedCfg<FMT>::SMEM, st);
+    cudaLaunchConfig_t cfg = at.config(dim3(grid), dim3(FusedCfg<FMT>::THREADS), FusedCfg<FMT>::SMEM, st);
     return cudaLaunchKernelEx(&cfg, fused_mlp_kernel<FMT>, a1, b1, a2, b2, a1s, a2s, p1, p2, fs);
 }
 
