@@ -547,22 +547,25 @@ def test_weight_transform_layout(fmt):
 
 # ----------------------------------------------------------------------------- failure detection
 
-@pytest.mark.parametrize("mode", ["fused", "split256", "pair"])
-def test_bounded_wait_timeout_reports_and_context_survives(mode):
+@pytest.mark.parametrize("fmt,mode", [("mxfp8", "fused"), ("mxfp8", "split256"), ("mxfp8", "pair"),
+                                      ("nvfp4", "fused")])
+def test_bounded_wait_timeout_reports_and_context_survives(fmt, mode):
     """A 1 ns limit makes the GEMM's pipeline waits run out: the kernel records
     MOE_ERR_TIMEOUT, waits for its own copies and MMAs, and returns. The status reads
-    back, and the same plan with the default limit then computes the same answer."""
-    shape = _small_case("mxfp8", T=256, H=2048, I=512, E=4, k=2)
+    back, and the same plan with the default limit then computes the same answer.
+    (The NVFP4 one-kernel GEMM also has the scale-factor warps' waits.)"""
+    shape = _small_case(fmt, T=256, H=2048, I=512, E=4, k=2)
     case = G.float_case(shape)
     run = G.run_gpu(case, **G.MODES[mode])
     good = G.out_f64(run)
+    a2 = run.inputs.get("a2")
     run.plan.set_wait_timeout(1)
     run.plan.forward(run.inputs["hidden"], run.inputs["topk_ids"], run.inputs["topk_weights"], run.kweights,
-                     workspace=run.workspace)
+                     l2_act_scale=a2, workspace=run.workspace)
     assert run.plan.last_status(run.workspace) == 7
     run.plan.set_wait_timeout(0)
     out = run.plan.forward(run.inputs["hidden"], run.inputs["topk_ids"], run.inputs["topk_weights"], run.kweights,
-                           workspace=run.workspace)
+                           l2_act_scale=a2, workspace=run.workspace)
     torch.cuda.synchronize()
     assert run.plan.last_status(run.workspace) == 0
     assert np.array_equal(out.float().cpu().numpy(), good)
