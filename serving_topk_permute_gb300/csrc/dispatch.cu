@@ -48,13 +48,29 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
     }
 }
 
+// 2^n exactly, for -149 <= n <= 127 (fp32 subnormals below 2^-126). x * pow2f(n) is then the
+// correctly rounded x * 2^n, the value ldexpf(x, n) returns, at the cost of one multiply
+// (this library builds with IEEE subnormals: no flush to zero).
+__device__ __forceinline__ float pow2f(int n) {
+    return n >= -126 ? __int_as_float((n + 127) << 23) : __int_as_float(1 << (n + 149));
+}
+
+// Row r's scale byte of block kb in the activation scale atoms (act_sf_offset) is
+// sf_row_base(r) + (kb / 4) * 512 + kb % 4: each atom holds 4 blocks of 128 rows, and the
+// atoms of a row tile follow one another in K order.
+__device__ __forceinline__ int64_t sf_row_base(int64_t r, int S, int64_t nks) {
+    return (r / BM) * nks * S * ATOM_BYTES + (r % 32) * 16 + ((r % BM) / 32) * 4;
+}
+__device__ __forceinline__ int64_t sf_byte(int64_t base, int kb) { return base + (int64_t)(kb >> 2) * ATOM_BYTES + (kb & 3); }
+
 // MXFP8 codes of one 8-element chunk (block exponent ex), as 8 bytes
 __device__ __forceinline__ uint2 mxfp8_chunk(const float (&f)[8], int ex) {
+    const float sc = pow2f(-ex);  // ex in [-127, 127]
     uint32_t w[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-        const uint32_t lo = cvt_e4m3x2(ldexpf(f[4 * i], -ex), ldexpf(f[4 * i + 1], -ex));
-        const uint32_t hi = cvt_e4m3x2(ldexpf(f[4 * i + 2], -ex), ldexpf(f[4 * i + 3], -ex));
+        const uint32_t lo = cvt_e4m3x2(f[4 * i] * sc, f[4 * i + 1] * sc);
+        const uint32_t hi = cvt_e4m3x2(f[4 * i + 2] * sc, f[4 * i + 3] * sc);
         w[i] = lo | (hi << 16);
     }
     return make_uint2(w[0], w[1]);
@@ -77,6 +93,7 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     const int nchunks = a.H / 8;
     __shared__ int s_rows[32];
+    __shared__ int64_t s_sfb[32];  // each row's scale-byte base in the atoms (sf_row_base)
     __shared__ int s_rank[32];  // rank of slot j among the equal ids before it in its routing chunk
     __shared__ int s_exp[32];
     __shared__ float s_amax[NT / 32];
@@ -162,18 +179,22 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
     grid_dep_wait();  // routing has written the chunk bases (and the previous forward is done with x_scale)
     grid_dep_launch();
     if (a.fmt == MOE_FMT_NVFP4 && tid == 0) a.x_scale[t] = gs;
+    const int S = fmt_sf_atoms(a.fmt);
     if (batched) {
-        if (tid == 0) s_rows[0] = t;
+        if (tid == 0) {
+            s_rows[0] = t;
+            s_sfb[0] = sf_row_base(t, S, fmt_k_stages(a.fmt, a.H));
+        }
     } else if (tid < a.k) {
         const int s = t * a.k + tid, e = s_exp[tid];
         const int r = e >= 0 && e < a.E ? a.wbase[s / chunk * a.E + e] + s_rank[tid] : -1;
         a.inv[s] = r;
         s_rows[tid] = r;
+        s_sfb[tid] = r >= 0 ? sf_row_base(r, S, fmt_k_stages(a.fmt, a.H)) : 0;
         if (r >= 0) a.src[r] = s;  // the routing kernel wrote the padding rows
     }
     __syncthreads();
     const int k = batched ? 1 : a.k;
-    const int64_t nks_x = fmt_k_stages(a.fmt, a.H);
 
 #pragma unroll
     for (int i = 0; i < MAXC; ++i) {
@@ -197,16 +218,16 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
             const int ex = ue8m0_exponent_fp4(amax);
+            const float sc = pow2f(-ex);  // ex in [-127, 127]
             uint32_t word = 0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                word |= cvt_e2m1x2(ldexpf(f[2 * j], -ex), ldexpf(f[2 * j + 1], -ex)) << (8 * j);
+            for (int j = 0; j < 4; ++j) word |= cvt_e2m1x2(f[2 * j] * sc, f[2 * j + 1] * sc) << (8 * j);
             if (in)
                 for (int j = 0; j < k; ++j) {
                     const int r = s_rows[j];
                     if (r < 0) continue;
                     reinterpret_cast<uint32_t*>(a.xq + (int64_t)r * (a.H / 2))[c] = word;
-                    if ((c & 3) == 0) a.xsf[act_sf_offset(r, c / 4, 2, nks_x)] = (uint8_t)(ex + 127);
+                    if ((c & 3) == 0) a.xsf[sf_byte(s_sfb[j], c / 4)] = (uint8_t)(ex + 127);
                 }
         } else if (a.fmt == MOE_FMT_MXFP8) {
             const int ex = mxfp8_block_exponent(f);
@@ -216,7 +237,7 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
                     const int r = s_rows[j];
                     if (r < 0) continue;
                     reinterpret_cast<uint2*>(a.xq + (int64_t)r * a.H)[c] = codes;
-                    if ((c & 3) == 0) a.xsf[act_sf_offset(r, c / 4, 1, nks_x)] = (uint8_t)(ex + 127);
+                    if ((c & 3) == 0) a.xsf[sf_byte(s_sfb[j], c / 4)] = (uint8_t)(ex + 127);
                 }
         } else {
             float amax = 0.0f;
@@ -236,7 +257,7 @@ __device__ __forceinline__ void dispatch_one(const DispatchArgs& a, const int t,
                     const int r = s_rows[j];
                     if (r < 0) continue;
                     reinterpret_cast<uint32_t*>(a.xq + (int64_t)r * (a.H / 2))[c] = word;
-                    if ((c & 1) == 0) a.xsf[act_sf_offset(r, c / 2, 4, nks_x)] = (uint8_t)sb;
+                    if ((c & 1) == 0) a.xsf[sf_byte(s_sfb[j], c / 2)] = (uint8_t)sb;
                 }
         }
         // unpermuted copy for the shared expert
