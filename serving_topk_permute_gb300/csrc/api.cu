@@ -540,7 +540,7 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
     if (d.fmt == MOE_FMT_NVFP4 && (!weights->w13_gs || !weights->w2_gs || !l2_act_scale)) return MOE_ERR_INVALID_ARG;
     if (d.Is > 0 && (!shared || !shared->w13 || !shared->w2)) return MOE_ERR_INVALID_ARG;
     if (d.Is > 0 && d.sfmt != MOE_FMT_BF16 && (!shared->w13_sf || !shared->w2_sf)) return MOE_ERR_INVALID_ARG;
-    if (c.post_norm && !norm_gamma) return MOE_ERR_INVALID_ARG;
+    if (c.post_norm && (!norm_gamma || !aligned(norm_gamma))) return MOE_ERR_INVALID_ARG;
     const Layout L = layout_of(c, T);
     if (workspace_bytes < (size_t)L.total) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;

@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 4) combine_kernel(const Combi
         float acc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+        // the shared expert's chunk, loaded beside the k rows' (added after them)
+        const uint4 vs = a.ys ? reinterpret_cast<const uint4*>(a.ys + (int64_t)t * a.H)[c] : make_uint4(0, 0, 0, 0);
         for (int j0 = 0; j0 < a.k; j0 += COMBINE_BATCH) {
             uint4 v[COMBINE_BATCH];
 #pragma unroll
@@ -80,7 +82,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 4) combine_kernel(const Combi
                 if (j < a.k && s_rows[j] >= 0) acc_bf16x8(acc, v[u], s_w[j]);
             }
         }
-        if (a.ys) acc_bf16x8(acc, reinterpret_cast<const uint4*>(a.ys + (int64_t)t * a.H)[c], 1.0f);
+        if (a.ys) acc_bf16x8(acc, vs, 1.0f);
         if (!norm) {
             orow[c] = pack_bf16x8(acc);
         } else {
@@ -102,9 +104,12 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 4) combine_kernel(const Combi
     for (int w = 0; w < COMBINE_THREADS / 32; ++w) tot += s_red[w];
     const float scale = 1.0f / sqrtf(tot / (float)a.H + a.eps);
     for (int c = tid; c < nchunks; c += COMBINE_THREADS) {
+        const float4 g0 = reinterpret_cast<const float4*>(a.gamma)[2 * c];  // gamma is 256-byte aligned
+        const float4 g1 = reinterpret_cast<const float4*>(a.gamma)[2 * c + 1];
+        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
         float v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = s_z[8 * c + j] * (a.gamma[8 * c + j] * scale);
+        for (int j = 0; j < 8; ++j) v[j] = s_z[8 * c + j] * (g[j] * scale);
         orow[c] = pack_bf16x8(v);
     }
 }

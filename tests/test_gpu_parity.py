@@ -345,6 +345,36 @@ def test_capacity_and_empty_batch():
     assert out.shape == (0, shape.H)
 
 
+def test_misaligned_pointers_refused():
+    """Every pointer the kernels read or write with 16-byte accesses must be 256-byte aligned:
+    a misaligned hidden, output or norm gamma is refused on the host (MOE_ERR_INVALID_ARG)
+    before anything is launched, and the plan then still computes the same answer."""
+    import serving_topk_permute_gb300 as pkg
+    case = G.float_case(REDUCED["nvfp4_shared_norm"])
+    run = G.run_gpu(case)
+    i = run.inputs
+    T, H = case.x.shape
+    big_h = torch.empty(T * H + 8, dtype=torch.bfloat16, device=G.dev())
+    big_o = torch.empty(T * H + 8, dtype=torch.bfloat16, device=G.dev())
+    big_g = torch.empty(H + 4, dtype=torch.float32, device=G.dev())
+    big_g[1:H + 1].copy_(i["gamma"])
+    bad = {"hidden": dict(hidden=big_h[8:].view(T, H).copy_(i["hidden"])),
+           "out": dict(out=big_o[8:].view(T, H)),
+           "gamma": dict(norm_gamma=big_g[1:H + 1])}
+    for what, kw in bad.items():
+        args = dict(hidden=i["hidden"], norm_gamma=i["gamma"], out=None)
+        args.update(kw)
+        with pytest.raises(pkg.MoeError) as e:
+            run.plan.forward(args["hidden"], i["topk_ids"], i["topk_weights"], run.kweights, l2_act_scale=i["a2"],
+                             shared=run.kshared, norm_gamma=args["norm_gamma"], out=args["out"],
+                             workspace=run.workspace)
+        assert e.value.status == 1, what
+    out = run.plan.forward(i["hidden"], i["topk_ids"], i["topk_weights"], run.kweights, l2_act_scale=i["a2"],
+                           shared=run.kshared, norm_gamma=i["gamma"], workspace=run.workspace)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), run.out.view(torch.int16))
+
+
 def test_workspace_too_small():
     import serving_topk_permute_gb300 as pkg
     shape = _small_case("bf16", T=16)
