@@ -101,3 +101,46 @@ def test_noalloc_binding_refuses_host_tensors(pkg):
         pkg.permute_noalloc(torch.zeros((4, 2), dtype=torch.int32), 8)
     with pytest.raises(ValueError):
         pkg.permute_noalloc(torch.zeros(8, dtype=torch.int32), 8)
+
+
+def _defines(prefix: str) -> dict:
+    """The #define constants of include/moe.h whose names start with prefix."""
+    out = {}
+    for m in re.finditer(r"^#define\s+(" + prefix + r"\w+)\s+(\d+)u?\b", open(HEADER).read(), flags=re.M):
+        out[m.group(1)] = int(m.group(2))
+    return out
+
+
+def _struct_fields(name: str) -> list:
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct " + name + r" \{(.*?)\}", text, flags=re.S).group(1)
+    return re.findall(r"(\w+)\s*;", body)
+
+
+def test_binding_constants_match_the_header(pkg):
+    """The Python binding restates the header's numbers: formats, flags, weight ids, workspace
+    regions, kernel timing slots, status codes, and the field order of the two structs it passes."""
+    from serving_topk_permute_gb300 import moe as M
+    fmts = _defines("MOE_FMT_")
+    assert {k: fmts["MOE_FMT_" + k.upper()] for k in M.FORMATS} == M.FORMATS
+    flags = _defines("MOE_FLAG_")
+    assert flags["MOE_FLAG_DEBUG_H"] == M.FLAG_DEBUG_H
+    assert flags["MOE_FLAG_TILE_128"] == M.FLAG_TILE[128] and flags["MOE_FLAG_TILE_256"] == M.FLAG_TILE[256]
+    assert flags["MOE_FLAG_CTA_PAIR"] == M.FLAG_CTA["pair"] and flags["MOE_FLAG_CTA_SINGLE"] == M.FLAG_CTA["single"]
+    assert flags["MOE_FLAG_SERIAL"] == M.FLAG_SERIAL and flags["MOE_FLAG_SPLIT_GEMM"] == M.FLAG_SPLIT_GEMM
+    w = _defines("MOE_W") | _defines("MOE_SHARED_W")
+    assert [w[n] for n in ("MOE_W13", "MOE_W13_SF", "MOE_W2", "MOE_W2_SF", "MOE_SHARED_W13", "MOE_SHARED_W13_SF",
+                           "MOE_SHARED_W2", "MOE_SHARED_W2_SF", "MOE_W13_GS", "MOE_W2_GS")] == [
+        M.W13, M.W13_SF, M.W2, M.W2_SF, M.SHARED_W13, M.SHARED_W13_SF, M.SHARED_W2, M.SHARED_W2_SF, M.W13_GS, M.W2_GS]
+    regions = _defines("MOE_REGION_")
+    names = {"counts": "COUNTS", "offsets": "OFFSETS", "src": "SRC", "inv_perm": "INV_PERM", "xq": "XQ", "xsf": "XSF",
+             "x_scale": "XSCALE", "hq": "HQ", "hsf": "HSF", "h_debug": "H_DEBUG", "y": "Y", "meta": "META",
+             "shared_y": "SHARED_Y"}
+    assert {k: regions["MOE_REGION_" + v] for k, v in names.items()} == M.REGIONS
+    kernels = _defines("MOE_KERNEL_")
+    assert [kernels["MOE_KERNEL_" + k.upper()] for k in M.KERNELS] == list(range(len(M.KERNELS)))
+    every = _defines("MOE_")
+    assert every["MOE_NUM_KERNELS"] == len(M.KERNELS)
+    assert every["MOE_OK"] == M.MOE_OK == 0
+    assert [f for f, _ in M.Config._fields_] == _struct_fields("moe_config")
+    assert [f for f, _ in M.Weights._fields_] == _struct_fields("moe_weights")
