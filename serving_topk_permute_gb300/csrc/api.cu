@@ -189,6 +189,13 @@ bool map_atoms(CUtensorMap* m, const void* base, uint64_t atoms, uint32_t box_at
 }
 
 bool aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+// every pointer a weight set carries is 256-byte aligned (null ones are checked elsewhere)
+bool weights_aligned(const moe_weights_t* w) {
+    for (const void* p : {(const void*)w->w13, (const void*)w->w13_sf, (const void*)w->w13_gs, (const void*)w->w2,
+                          (const void*)w->w2_sf, (const void*)w->w2_gs})
+        if (p && !aligned(p)) return false;
+    return true;
+}
 
 }  // namespace
 
@@ -363,7 +370,7 @@ static int transform(const moe_config_t& c, int fmt, int E, int I, const moe_wei
                      bool gscales, cudaStream_t st) {
     const int H = c.hidden;
     if (!src || !dst || !src->w13 || !src->w2 || !dst->w13 || !dst->w2) return MOE_ERR_INVALID_ARG;
-    if (!aligned(src->w13) || !aligned(src->w2) || !aligned(dst->w13) || !aligned(dst->w2)) return MOE_ERR_INVALID_ARG;
+    if (!weights_aligned(src) || !weights_aligned(dst)) return MOE_ERR_INVALID_ARG;
     if (src->w13 == dst->w13 || src->w2 == dst->w2) return MOE_ERR_INVALID_ARG;
     const bool scaled = fmt != MOE_FMT_BF16;
     if (scaled && (!src->w13_sf || !src->w2_sf || !dst->w13_sf || !dst->w2_sf)) return MOE_ERR_INVALID_ARG;
@@ -541,6 +548,8 @@ int moe_forward(moe_plan_t plan, int32_t T, const void* hidden, const int32_t* t
     if (d.Is > 0 && (!shared || !shared->w13 || !shared->w2)) return MOE_ERR_INVALID_ARG;
     if (d.Is > 0 && d.sfmt != MOE_FMT_BF16 && (!shared->w13_sf || !shared->w2_sf)) return MOE_ERR_INVALID_ARG;
     if (c.post_norm && (!norm_gamma || !aligned(norm_gamma))) return MOE_ERR_INVALID_ARG;
+    if (!weights_aligned(weights) || (d.Is > 0 && !weights_aligned(shared))) return MOE_ERR_INVALID_ARG;
+    if (d.fmt == MOE_FMT_NVFP4 && !aligned(l2_act_scale)) return MOE_ERR_INVALID_ARG;
     const Layout L = layout_of(c, T);
     if (workspace_bytes < (size_t)L.total) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
@@ -683,6 +692,7 @@ int moe_forward_batched(moe_plan_t plan, int32_t max_tokens, const void* hidden,
     if (!weights->w13 || !weights->w2) return MOE_ERR_INVALID_ARG;
     if (d.fmt != MOE_FMT_BF16 && (!weights->w13_sf || !weights->w2_sf)) return MOE_ERR_INVALID_ARG;
     if (d.fmt == MOE_FMT_NVFP4 && (!weights->w13_gs || !weights->w2_gs || !l2_act_scale)) return MOE_ERR_INVALID_ARG;
+    if (!weights_aligned(weights) || (d.fmt == MOE_FMT_NVFP4 && !aligned(l2_act_scale))) return MOE_ERR_INVALID_ARG;
     const BLayout L = batched_layout_of(c, max_tokens);
     if (workspace_bytes < (size_t)L.total) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;

@@ -346,9 +346,10 @@ def test_capacity_and_empty_batch():
 
 
 def test_misaligned_pointers_refused():
-    """Every pointer the kernels read or write with 16-byte accesses must be 256-byte aligned:
-    a misaligned hidden, output or norm gamma is refused on the host (MOE_ERR_INVALID_ARG)
-    before anything is launched, and the plan then still computes the same answer."""
+    """Every device pointer must be 256-byte aligned (the kernels read and write with 16-byte
+    and bulk copies): a misaligned hidden, output, norm gamma, scale-atom tensor or L2 input
+    scale is refused on the host (MOE_ERR_INVALID_ARG) before anything is launched, and the
+    plan then still computes the same answer."""
     import serving_topk_permute_gb300 as pkg
     case = G.float_case(REDUCED["nvfp4_shared_norm"])
     run = G.run_gpu(case)
@@ -358,14 +359,20 @@ def test_misaligned_pointers_refused():
     big_o = torch.empty(T * H + 8, dtype=torch.bfloat16, device=G.dev())
     big_g = torch.empty(H + 4, dtype=torch.float32, device=G.dev())
     big_g[1:H + 1].copy_(i["gamma"])
+    sf = run.kweights["w13_sf"]
+    big_sf = torch.empty(sf.numel() + 16, dtype=torch.uint8, device=G.dev())
+    big_a2 = torch.empty(8, dtype=torch.float32, device=G.dev())
+    big_a2[1:2].copy_(i["a2"])
     bad = {"hidden": dict(hidden=big_h[8:].view(T, H).copy_(i["hidden"])),
            "out": dict(out=big_o[8:].view(T, H)),
-           "gamma": dict(norm_gamma=big_g[1:H + 1])}
+           "gamma": dict(norm_gamma=big_g[1:H + 1]),
+           "scale atoms": dict(weights={**run.kweights, "w13_sf": big_sf[16:].copy_(sf)}),
+           "L2 input scale": dict(a2=big_a2[1:2])}
     for what, kw in bad.items():
-        args = dict(hidden=i["hidden"], norm_gamma=i["gamma"], out=None)
+        args = dict(hidden=i["hidden"], norm_gamma=i["gamma"], out=None, weights=run.kweights, a2=i["a2"])
         args.update(kw)
         with pytest.raises(pkg.MoeError) as e:
-            run.plan.forward(args["hidden"], i["topk_ids"], i["topk_weights"], run.kweights, l2_act_scale=i["a2"],
+            run.plan.forward(args["hidden"], i["topk_ids"], i["topk_weights"], args["weights"], l2_act_scale=args["a2"],
                              shared=run.kshared, norm_gamma=args["norm_gamma"], out=args["out"],
                              workspace=run.workspace)
         assert e.value.status == 1, what
